@@ -1,0 +1,113 @@
+"""Each plausible mistake planted in a copy of the oracle source must fail at
+least one of the oracle's pins (so the pins really constrain the oracle).
+
+The mistakes are planted by text substitution in a temporary copy of
+``oracle/moe_oracle.cpp`` compiled on the CPU; the oracle itself is untouched.
+"""
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_finalize as tf
+import test_oracle_index as ti
+import test_oracle_route as tr
+
+ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
+
+MUTANTS = {
+    "group score = top-1 only": (
+        "g[j] = (S == 1) ? group_vals[0] : group_vals[0] + group_vals[1];",
+        "g[j] = group_vals[0];"),
+    "group ties to the higher index": (
+        "if (g[x] != g[y]) return g[x] > g[y];\n      return x < y;",
+        "if (g[x] != g[y]) return g[x] > g[y];\n      return x > y;"),
+    "expert ties to the higher index": (
+        "if (b[x] != b[y]) return b[x] > b[y];\n      return x < y;",
+        "if (b[x] != b[y]) return b[x] > b[y];\n      return x > y;"),
+    "groups kept in index order": (
+        "const int32_t j = group_order[m];", "const int32_t j = m;"),
+    "bias kept in the weights": ("w[k] = s[allowed[k]];", "w[k] = b[allowed[k]];"),
+    "normalisation dropped": ("w[k] = w[k] / sum;", "w[k] = w[k];"),
+    "scale applied twice": ("w[k] = w[k] / sum;", "w[k] = w[k] / sum * scale;"),
+    "bias subtracted": ("b[e] = s[e] + bias[e];", "b[e] = s[e] - bias[e];"),
+    "unstable placement (reverse walk)": (
+        "for (int64_t i = 0; i < N; ++i) {\n    const uint32_t pos",
+        "for (int64_t i = N - 1; i >= 0; --i) {\n    const uint32_t pos"),
+    "restore transposed": ("restore_token_order[i] = pos;", "restore_token_order[pos] = i;"),
+    "CSR tail left at zero": ("expert_start_indices[j] = static_cast<uint32_t>(N);",
+                              "expert_start_indices[j] = 0;"),
+    "stats swapped": ("expert_usage_stats[0] = max_count;\n  expert_usage_stats[1] = active;",
+                      "expert_usage_stats[0] = active;\n  expert_usage_stats[1] = max_count;"),
+    "finalize drops the first term": (
+        "for (int32_t k = 0; k < K; ++k) {\n      const int64_t row = restore[t * K + k];\n"
+        "      acc = std::fma",
+        "for (int32_t k = 1; k < K; ++k) {\n      const int64_t row = restore[t * K + k];\n"
+        "      acc = std::fma"),
+    "finalize restore indexed k-major": (
+        "const int64_t row = restore[t * K + k];\n      acc = std::fma(w[t * K + k]",
+        "const int64_t row = restore[k * T + t];\n      acc = std::fma(w[t * K + k]"),
+    "finalize weight indexed k-major": (
+        "acc = std::fma(w[t * K + k], bf16", "acc = std::fma(w[k * T + t], bf16"),
+    "finalize reads down transposed": ("down[row * H + h]), acc)", "down[h * T * K + row]), acc)"),
+}
+
+
+def _pins():
+    """The oracle's pins, as plain callables (all CPU, a few seconds in total)."""
+    return [
+        lambda: tr.test_golden_fixtures("route_group_limited.json"),
+        lambda: tr.test_golden_fixtures("route_ungrouped_no_norm.json"),
+        tr.test_brute_force_tiny_workload,
+        lambda: tr.test_brute_force_random(12, 3, 2, 4, True),
+        lambda: tr.test_brute_force_random(8, 1, 1, 2, False),
+        lambda: tr.test_tie_stress_brute_force("quantised"),
+        tr.test_all_equal_scores_pick_lowest_indices,
+        tr.test_bias_changes_selection_but_not_weights,
+        ti.test_golden_fixture,
+        lambda: ti.test_random_ids(1000, 64),
+        ti.test_all_slots_on_one_expert,
+        tf.test_golden_fixture,
+        tf.test_permutation_copy_closed_form,
+        lambda: tf.test_library_gather_weighted_sum(33, 8, 256),
+        lambda: tf.test_library_gather_weighted_sum(17, 3, 72),
+        tf.test_tiny_workload_chain,
+    ]
+
+
+def _build_mutant(tmpdir, old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    path = os.path.join(tmpdir, "mutant.cpp")
+    with open(path, "w") as fh:
+        fh.write(src.replace(old, new))
+    # the copy includes the real header
+    inc = os.path.dirname(ORACLE_SRC)
+    so = os.path.join(tmpdir, "libmutant.so")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-I", inc, "-o", so, path], check=True)
+    return so
+
+
+def test_pins_pass_on_the_real_oracle():
+    for pin in _pins():
+        pin()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    old, new = MUTANTS[name]
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _build_mutant(tmp, old, new)
+        caught = []
+        with oracle.using_library(so):
+            for pin in _pins():
+                try:
+                    with np.errstate(all="ignore"):
+                        pin()
+                except (AssertionError, oracle.OracleError, ValueError, IndexError):
+                    caught.append(pin)
+        assert caught, f"no pin caught the planted mistake: {name}"
