@@ -1,0 +1,421 @@
+"""Benchmark of the MoE routing hot path: route -> create_indices -> finalize.
+
+One step = the three stages over one batch of seeded synthetic input
+(default: the DeepSeek-V3-shaped prefill workload, T=16384 tokens, E=256
+experts in 8 groups, top-4 groups, K=8, H=7168), inputs resident in HBM,
+L2 flushed (a 256 MB write) before every step outside the timed events.
+
+Prints ONE JSON line. `value` is whole-job tokens/s from CUDA-event device
+time per step; `e2e` is the same metric through the host-buffer call
+(pinned host inputs copied in, output copied back, every step); `roofline`
+is the finalize kernel's algorithmic bytes / its event-timed duration
+against the measured HBM copy bandwidth; `cpu_baseline` is the CPU oracle
+on the host cores. `--impl reference` times only the CPU oracle.
+
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling), with no
+collective on the data path; the barrier and max-over-ranks only bracket
+the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "route+index+finalize tokens/s; finalize & router HBM GB/s vs ~8 TB/s peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--config", default="dsv3_prefill")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's token count (profiling runs)")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (the timing reduction; not on the data path)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, worst_ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch in each step."""
+    return tokens_per_rank * world / (worst_ms_per_step * 1e-3)
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+            return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(cfg):
+    N = cfg.T * cfg.K
+    return {
+        "route": 4 * cfg.T * cfg.E + 4 * cfg.E + 8 * cfg.T * cfg.K,
+        "index": 4 * N + 8 * N + 4 * (cfg.E + 1) + 4 * cfg.E + 8,
+        "finalize": 2 * N * cfg.H + 4 * N + 4 * N + 2 * cfg.T * cfg.H,
+    }
+
+
+def profile_traffic(kernel_file: str, summary_name: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source's hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", summary_name)
+    src = os.path.join(ROOT, "moe_token_routing_gb300", "csrc", kernel_file)
+    try:
+        fields = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if fields.get("source_sha256_16") != digest:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and self.uuid not in parts[0] and parts[0] not in self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def device_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_chain_seconds(cfg, scores, bias, down, t0: int, n_tok: int) -> float:
+    """Oracle route -> index -> finalize over tokens [t0, t0+n_tok); returns seconds."""
+    import oracle
+    s = scores[t0:t0 + n_tok]
+    start = time.perf_counter()
+    ids, w = oracle.route(s, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    idx = oracle.create_indices(ids, cfg.E)
+    N = n_tok * cfg.K
+    oracle.finalize(down[:N], idx["restore_token_order"], w, n_tok, cfg.K, cfg.H)
+    return time.perf_counter() - start
+
+
+def cpu_baseline(cfg, scores, bias, down, target_s: float):
+    """The oracle as it stands (single thread) on a bounded sample of the workload."""
+    probe_tok = min(cfg.T, 256)
+    probe = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok)
+    per_tok = max(probe / probe_tok, 1e-9)
+    n_tok = int(min(cfg.T, max(1, target_s / per_tok)))
+    reps, total, done = 0, 0.0, 0
+    while total < target_s and reps < 8:
+        total += oracle_chain_seconds(cfg, scores, bias, down, 0, n_tok)
+        done += n_tok
+        reps += 1
+    return {"value": done / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{cfg.name}: tokens 0..{n_tok - 1} of {cfg.T}, route+index+finalize, "
+                      f"{reps} pass(es), {total:.1f} s single-threaded"}
+
+
+def host_inputs(cfg, seed_offset=0, pinned=False):
+    import numpy as np
+    import torch
+
+    import synth
+    c = cfg.replace(seed=cfg.seed + seed_offset)
+    scores = synth.make_scores(c)
+    bias = synth.make_bias(c)
+    down_t = torch.empty((c.N, c.H), dtype=torch.bfloat16, pin_memory=pinned)
+    synth.make_down(c, out_ptr=down_t.data_ptr())
+    down_np = down_t.view(torch.int16).numpy().view(np.uint16)
+    return scores, bias, down_t, down_np
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    scores, bias, _, down = host_inputs(cfg)
+    probe_tok = min(cfg.T, 256)
+    per_tok = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok) / probe_tok
+    budget = 150.0  # seconds for warmup + timed steps
+    n_tok = int(max(1, min(cfg.T, budget / max(1, args.steps + args.warmup) / max(per_tok, 1e-9))))
+    t0 = 0
+    for _ in range(args.warmup):
+        oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok)
+        t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok)
+        t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
+    value = n_tok * args.steps / total
+    sample = f"{cfg.name}: {n_tok} of {cfg.T} tokens per step, route+index+finalize, single thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": config_dict(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name, "tokens": cfg.T, "n_routed_experts": cfg.E,
+            "n_groups": cfg.G, "topk_group": cfg.M, "n_experts_per_tok": cfg.K,
+            "hidden": cfg.H, "norm_weights": cfg.norm_weights,
+            "routed_scaling_factor": cfg.scale, "scores": cfg.scores, "bias": cfg.bias,
+            "down_dtype": "bf16", "weights_dtype": "f32", "output_dtype": "bf16",
+            "l2": "flushed before every step (256 MB write, outside the timed events)"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, cfg, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import moe_token_routing_gb300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    moe.load_library()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    scores, bias, down_h, down_np = host_inputs(cfg, seed_offset=rank, pinned=True)
+    s_d = torch.from_numpy(scores).to(dev)
+    b_d = torch.from_numpy(bias).to(dev)
+    d_d = down_h.to(dev)
+    pipe = moe.RoutingPipeline(cfg.T, cfg.E, cfg.K, cfg.H, cfg.G, cfg.M, cfg.norm_weights,
+                               cfg.scale, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        pipe(s_d, b_d, d_d)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(device_uuid(dev))
+    sampler.start()
+    time.sleep(0.25)
+    barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        pipe.route(s_d, b_d)
+        e[1].record(stream)
+        pipe.create_indices()
+        e[2].record(stream)
+        pipe.finalize(d_d)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    route_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    index_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    fin_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    mean_step = statistics.fmean(step_ms)
+
+    # whole-job throughput: max over ranks of the mean step time
+    worst_ms = max_over_ranks(mean_step, world, dev)
+
+    # correctness spot check of this run's output against the first token rows
+    out_ok = bool(torch.isfinite(pipe.output[:4].float()).all().item())
+
+    # ---- end to end through the host-buffer call
+    out_h = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, pin_memory=True)
+    s_h = torch.from_numpy(scores).pin_memory()
+    b_h = torch.from_numpy(bias).pin_memory()
+    pipe.run_host(s_h, b_h, down_h, out_h)
+    torch.cuda.synchronize(dev)
+    ke = max(1, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(ke):
+        pipe.run_host(s_h, b_h, down_h, out_h)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
+    h2d, d2h = pipe.host_bytes()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    nbytes = algorithmic_bytes(cfg)
+    peak, peak_kind = measured_hbm_peak()
+    fin_mean = statistics.fmean(fin_ms)
+    route_mean = statistics.fmean(route_ms)
+    fin_gbs = nbytes["finalize"] / (fin_mean * 1e-3) / 1e9
+    route_gbs = nbytes["route"] / (route_mean * 1e-3) / 1e9
+    launches_per_step = 1 + (1 if cfg.N <= 2048 else 3) + 1
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, scores, bias, down_np, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC,
+        "value": job_tokens_per_s(cfg.T, world, worst_ms),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": worst_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded)",
+        "config": config_dict(cfg),
+        "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": fin_gbs, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": fin_gbs / peak,
+                     "frac_vs_nominal_8tbs": fin_gbs / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": nbytes["finalize"],
+                     "traffic": profile_traffic("finalize.cu", "finalize_dsv3_prefill.txt")
+                     if cfg.name == "dsv3_prefill" else None},
+        "router_roofline": {"bound": "hbm", "achieved": route_gbs, "peak": peak, "unit": "GB/s",
+                            "frac": route_gbs / peak,
+                            "frac_vs_nominal_8tbs": route_gbs / NOMINAL_HBM_GBS,
+                            "algorithmic_bytes_per_launch": nbytes["route"]},
+        "stages_ms": {"route": route_mean, "create_indices": statistics.fmean(index_ms),
+                      "finalize": fin_mean, "step_median": statistics.median(step_ms)},
+        "stages_tokens_per_s": {"route": cfg.T / (route_mean * 1e-3),
+                                "create_indices": cfg.T / (statistics.fmean(index_ms) * 1e-3),
+                                "finalize": cfg.T / (fin_mean * 1e-3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "output_finite": out_ok,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    cfg = synth.get_config(args.config)
+    if args.tokens is not None:
+        cfg = cfg.replace(T=args.tokens)
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        return
+    run_gpu(args, cfg, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * moe_routing.h -- C ABI of libmoe_routing.so, the GB300 (sm_103a) MoE
+ * routing and combine hot path: group-limited top-k router, expert index
+ * builder, and fused unpermute + weighted top-k sum.
+ *
+ * Sources (Mojo kernel library API pages, cited by page title and section):
+ *   "group_limited_router_kernel"  -> moe_route
+ *   "moe_create_indices"           -> moe_create_indices
+ *   "moe_finalize"                 -> moe_finalize
+ *
+ * Conventions for every entry point:
+ *   - Argument order follows the pages: outputs first, then inputs, then the
+ *     sizes that the pages carry as tensor shapes or compile-time parameters,
+ *     then the CUDA stream that replaces the pages' DeviceContext.
+ *   - Every pointer is a DEVICE pointer to a dense row-major buffer owned by
+ *     the caller. The library allocates nothing, frees nothing and keeps no
+ *     state between calls; the index builder's scratch space is a
+ *     caller-provided workspace.
+ *   - Every call only enqueues work on `stream` (0 = the legacy default
+ *     stream) and returns without synchronising, except
+ *     moe_read_device_status, which waits for the stream.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and reported as a moe_status_t. MOE_ERR_CUDA means a launch failed
+ *     (cudaGetLastError after the launch). Errors found in the DATA (an
+ *     expert id outside [0, n_experts)) are recorded in a device status word
+ *     and never trap; see moe_read_device_status.
+ *   - A call with zero tokens / slots is valid.
+ */
+#ifndef MOE_ROUTING_H
+#define MOE_ROUTING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw bf16 bit pattern (1 sign, 8 exponent, 7 mantissa bits), as in __nv_bfloat16. */
+typedef uint16_t moe_bf16_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
+  MOE_ERR_INVALID_ARG = 2,  /* sizes inconsistent with the method (e.g. E % n_groups != 0) */
+  MOE_ERR_MISALIGNED = 3,   /* a pointer breaks the stated alignment */
+  MOE_ERR_UNSUPPORTED = 4,  /* valid for the method but outside this library's limits */
+  MOE_ERR_CUDA = 5,         /* a CUDA launch or copy failed */
+  MOE_ERR_WORKSPACE = 6     /* workspace NULL or smaller than the size query returns */
+} moe_status_t;
+
+/* Bits of the device status word written by moe_create_indices. */
+#define MOE_DEVICE_STATUS_BAD_EXPERT_ID 0x1u /* some topk_ids entry was outside [0, E) */
+
+/* Limits of this implementation. */
+#define MOE_MAX_EXPERTS 1024       /* n_routed_experts / n_experts */
+#define MOE_MAX_GROUPS 32          /* n_groups */
+#define MOE_MAX_EXPERTS_PER_TOK 32 /* n_experts_per_tok / num_experts_per_token */
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+/*
+ * moe_route -- group-limited top-k router.
+ * Page "group_limited_router_kernel": description paragraph; Parameters
+ * n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights;
+ * Args expert_indices, expert_weights, expert_scores, expert_bias,
+ * routed_scaling_factor.
+ *
+ * For each token t (row of expert_scores):
+ *   b[e]  = expert_scores[t,e] + expert_bias[e]           (fp32, selection only)
+ *   g[j]  = largest + second-largest b[e] of group j       (group j = experts
+ *           j*S .. j*S+S-1, S = E / n_groups; g[j] = b if S == 1)
+ *   keep the topk_group groups with the largest g (ties -> lower group index)
+ *   expert_indices[t,:] = the n_experts_per_tok experts of the kept groups
+ *           with the largest b, in that order (ties -> lower expert index)
+ *   expert_weights[t,k] = expert_scores[t, expert_indices[t,k]]; if
+ *           norm_weights, divided by their fp32 sum taken in k order; then
+ *           multiplied by routed_scaling_factor. All fp32, round-to-nearest.
+ *
+ * expert_indices  [T, K] int32 out.   expert_weights [T, K] fp32 out.
+ * expert_scores   [T, E] fp32 in.     expert_bias    [E] fp32 in.
+ * Requirements: 1 <= E <= MOE_MAX_EXPERTS; 1 <= n_groups <= MOE_MAX_GROUPS and
+ * E % n_groups == 0; 1 <= topk_group <= n_groups; 1 <= K <= topk_group * S and
+ * K <= MOE_MAX_EXPERTS_PER_TOK; T >= 0. 4-byte aligned pointers (16-byte
+ * alignment of expert_scores with E % 4 == 0 enables vector loads). Scores and
+ * bias must be free of NaN (the selection is then unspecified, never faulting).
+ */
+moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
+                       const float* expert_scores, const float* expert_bias,
+                       int64_t num_tokens, int32_t n_routed_experts, int32_t n_experts_per_tok,
+                       int32_t n_groups, int32_t topk_group, int32_t norm_weights,
+                       float routed_scaling_factor, cudaStream_t stream);
+
+/*
+ * Workspace bytes that moe_create_indices needs for num_slots slots and
+ * n_experts experts (always >= 256). Host-only; never fails (returns 0 for
+ * negative num_slots or n_experts outside [1, MOE_MAX_EXPERTS]).
+ */
+size_t moe_create_indices_workspace_size(int64_t num_slots, int32_t n_experts);
+
+/*
+ * moe_create_indices -- bucket sort of the flat router output by expert.
+ * Page "moe_create_indices": description paragraph (bucket sort so that each
+ * expert's tokens are contiguous); Parameters expected_count (no per-expert
+ * limit here); Args token_expert_order, expert_start_indices,
+ * restore_token_order, expert_ids, expert_usage_stats, topk_ids,
+ * scales_offset_p.
+ *
+ * Slot i = t*K + k of the flattened topk_ids [T, K] (num_slots = T*K):
+ *   token_expert_order [N]  uint32 out: slot indices grouped by expert, experts
+ *        in ascending id, ascending slot index within one expert (stable).
+ *   restore_token_order [N] uint32 out: position of slot i in
+ *        token_expert_order (its inverse permutation).
+ *   expert_ids [E] int32 out: the A active experts (count > 0) in ascending
+ *        id, then -1 in entries A .. E-1.
+ *   expert_start_indices [E+1] uint32 out: compact CSR over expert_ids: entry j
+ *        < A is where expert_ids[j]'s slots start, entries A .. E are N.
+ *   expert_usage_stats [2] uint32 out: {max slots on one expert, A}.
+ *   topk_ids [N] int32 in: expert id of each slot.
+ * workspace: device buffer of at least moe_create_indices_workspace_size()
+ *   bytes, 256-byte aligned, caller-owned; its first 4 bytes receive the
+ *   device status word. Calls sharing one workspace must not overlap.
+ * scales_offset_p must be NULL (block-scaled offsets are not provided).
+ * Requirements: 0 <= N < 2^32 - 1; 1 <= E <= MOE_MAX_EXPERTS; 4-byte aligned
+ * buffers. Out-of-range ids set MOE_DEVICE_STATUS_BAD_EXPERT_ID, are left out
+ * of every output count and leave the contents of the outputs unspecified.
+ */
+moe_status_t moe_create_indices(uint32_t* token_expert_order, uint32_t* expert_start_indices,
+                                uint32_t* restore_token_order, int32_t* expert_ids,
+                                uint32_t* expert_usage_stats, const int32_t* topk_ids,
+                                int64_t num_slots, int32_t n_experts, void* workspace,
+                                size_t workspace_bytes, uint32_t* scales_offset_p,
+                                cudaStream_t stream);
+
+/*
+ * moe_finalize -- fused unpermute gather + top-k weighted row sum.
+ * Page "moe_finalize": description paragraph (gather each token's K rows of
+ * down through restore_order, scale by the router weight, accumulate in
+ * fp32, never materialise [T, K, H]); Args output, down, restore_order,
+ * router_weight.
+ *
+ *   output[t,h] = bf16_rn( sum_{k=0}^{K-1} router_weight[t,k] *
+ *                          float(down[restore_order[t*K+k], h]) )
+ * accumulated in fp32 in k order with fused multiply-add from 0.
+ *
+ * output [T, H] bf16 out. down [T*K, H] bf16 in, rows in token_expert_order
+ * order. restore_order [T*K] uint32 in. router_weight [T, K] fp32 in.
+ * Requirements: T >= 0; 1 <= K <= MOE_MAX_EXPERTS_PER_TOK; T*K < 2^32; H >= 0
+ * and H % 8 == 0; output and down 16-byte aligned; restore_order and
+ * router_weight 4-byte aligned; output must not overlap down. A
+ * restore_order entry >= T*K is skipped (contributes nothing) and never read.
+ */
+moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
+                          const uint32_t* restore_order, const float* router_weight,
+                          int64_t num_tokens, int32_t num_experts_per_token, int64_t hidden,
+                          cudaStream_t stream);
+
+/*
+ * Reads the device status word that the last moe_create_indices call on
+ * `workspace` wrote (0 = clean; MOE_DEVICE_STATUS_* bits otherwise). Enqueues
+ * a 4-byte copy on `stream` and waits for the stream to finish.
+ */
+moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,
+                                    cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTING_H */

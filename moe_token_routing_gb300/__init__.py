@@ -1,0 +1,18 @@
+"""GB300-native (sm_103a) MoE routing and combine hot path.
+
+route (group-limited top-k router) -> create_indices (stable bucket sort by
+expert) -> finalize (fused unpermute + weighted top-k sum), each a CUDA
+kernel behind the C ABI of libmoe_routing.so (include/moe_routing.h).
+"""
+from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, EXPORTED_SYMBOLS, IndexBuffers, MoeError,
+                      MoeLibraryMissing, create_indices, finalize, load_library,
+                      moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
+                      moe_read_device_status, moe_route, route)
+from .pipeline import RoutingPipeline
+
+__all__ = [
+    "DEVICE_STATUS_BAD_EXPERT_ID", "EXPORTED_SYMBOLS", "IndexBuffers", "MoeError",
+    "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
+    "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
+    "moe_read_device_status", "moe_route", "route",
+]

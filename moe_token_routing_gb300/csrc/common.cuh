@@ -1,0 +1,40 @@
+// Shared device/host helpers of the sm_103a MoE routing kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_routing.h"
+
+namespace moe {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Order-preserving map of an fp32 value to uint32: a > b (IEEE, finite) iff
+// key(a) > key(b) as unsigned. -0 is folded to +0 first so that the two
+// zeros compare equal, as IEEE comparison does. Key 0 is below every
+// non-NaN value and marks "no candidate".
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Per-device properties looked up once.
+struct DeviceInfo {
+  int sm_count;
+};
+DeviceInfo device_info();
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline moe_status_t launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,381 @@
+// Expert index builder for sm_103a: a stable bucket sort of the flat router
+// output by expert id.
+//
+// Page "moe_create_indices", description paragraph: slots are grouped by
+// expert so that each expert's tokens are contiguous for the grouped matmul;
+// Args token_expert_order, expert_start_indices, restore_token_order,
+// expert_ids, expert_usage_stats, topk_ids. Parameters expected_count: the
+// pages' kernel caches a bounded number of slots per expert in shared memory;
+// here positions are computed arithmetically, so any count per expert works.
+//
+// Design (no inter-CTA waits, deterministic, stable):
+//   count   : CTA b counts the experts of its 2048 slots (warp-aggregated with
+//             match.any, shared-memory counters) -> counts[b][e].
+//   scan    : one CTA turns counts into bases: base[b][e] = start(e) +
+//             sum_{b' < b} counts[b'][e], and writes the compact CSR,
+//             expert_ids, usage stats and the device status word.
+//   scatter : CTA b re-reads its slots; within a CTA each warp owns 256
+//             consecutive slots, so a slot's position is base[b][e] + (slots of
+//             e in earlier warps) + (slots of e in earlier steps of its warp) +
+//             (lower lanes of its step with the same e). Writes
+//             token_expert_order and restore_token_order in one pass.
+//   For N <= 2048 one CTA does all three in one launch.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kIdxThreads = 256;
+constexpr int kIdxWarps = kIdxThreads / 32;
+constexpr int kStepsPerWarp = 8;
+constexpr int kSlotsPerWarp = 32 * kStepsPerWarp;
+constexpr int kSlotsPerCta = kIdxWarps * kSlotsPerWarp;  // 2048
+constexpr int kScanThreads = 1024;
+constexpr size_t kHeaderBytes = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  int64_t num_blocks;
+  size_t flags_off, counts_off, total;
+};
+
+Layout workspace_layout(int64_t N, int E) {
+  Layout L;
+  L.num_blocks = (N + kSlotsPerCta - 1) / kSlotsPerCta;
+  L.flags_off = kHeaderBytes;
+  if (L.num_blocks <= 1) {
+    L.counts_off = kHeaderBytes;
+    L.total = kHeaderBytes;
+  } else {
+    L.counts_off = L.flags_off + align256(sizeof(uint32_t) * (size_t)L.num_blocks);
+    L.total = L.counts_off + align256(sizeof(uint32_t) * (size_t)L.num_blocks * (size_t)E);
+  }
+  return L;
+}
+
+struct IdxArgs {
+  const int32_t* ids;
+  uint32_t* token_expert_order;
+  uint32_t* expert_start_indices;
+  uint32_t* restore_token_order;
+  int32_t* expert_ids;
+  uint32_t* stats;
+  uint32_t* status;  // workspace word 0
+  uint32_t* flags;   // [num_blocks]
+  uint32_t* counts;  // [num_blocks][E], overwritten with bases by the scan
+  uint32_t N;
+  int E;
+  int num_blocks;
+};
+
+// ---------------------------------------------------------------- block helpers
+// Exclusive prefix sum of data[0..n) in shared memory, in place; all threads of
+// the block call it. Returns the total.
+__device__ uint32_t block_exclusive_scan(uint32_t* data, int n, uint32_t* warp_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int beg = min((int)threadIdx.x * per, n), end = min(beg + per, n);
+  uint32_t local = 0;
+  for (int i = beg; i < end; ++i) local += data[i];
+  uint32_t x = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFullMask, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t v = lane < nwarps ? warp_tmp[lane] : 0u;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, v, off);
+      if (lane >= off) v += y;
+    }
+    warp_tmp[lane] = v;
+  }
+  __syncthreads();
+  uint32_t run = x - local + (warp > 0 ? warp_tmp[warp - 1] : 0u);
+  const uint32_t total = warp_tmp[nwarps - 1];
+  for (int i = beg; i < end; ++i) {
+    const uint32_t v = data[i];
+    data[i] = run;
+    run += v;
+  }
+  __syncthreads();
+  return total;
+}
+
+__device__ uint32_t block_max(uint32_t v, uint32_t* warp_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = __reduce_max_sync(kFullMask, v);
+  if (lane == 0) warp_tmp[warp] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  for (int w = 0; w < nwarps; ++w) r = max(r, warp_tmp[w]);
+  __syncthreads();
+  return r;
+}
+
+// Given per-expert totals tot[0..E) in shared memory: writes the compact CSR,
+// expert_ids and usage stats, and turns tot[] into each expert's start offset.
+// `act` is E words of shared scratch.
+__device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act,
+                                  uint32_t* warp_tmp) {
+  uint32_t local_max = 0;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    act[e] = tot[e] > 0u;
+    local_max = max(local_max, tot[e]);
+  }
+  __syncthreads();
+  const uint32_t max_count = block_max(local_max, warp_tmp);
+  const uint32_t active = block_exclusive_scan(act, a.E, warp_tmp);
+  block_exclusive_scan(tot, a.E, warp_tmp);  // tot[e] := start of expert e
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    const bool is_active = (e + 1 < a.E ? act[e + 1] : active) != act[e];
+    if (is_active) {
+      a.expert_ids[act[e]] = e;
+      a.expert_start_indices[act[e]] = tot[e];
+    }
+  }
+  for (int j = (int)active + threadIdx.x; j <= a.E; j += blockDim.x) {
+    a.expert_start_indices[j] = a.N;
+    if (j < a.E) a.expert_ids[j] = -1;
+  }
+  if (threadIdx.x == 0) {
+    a.stats[0] = max_count;
+    a.stats[1] = active;
+  }
+}
+
+// Loads this warp's slots: -1 marks a slot past N or an id outside [0, E).
+__device__ __forceinline__ void load_warp_slots(const IdxArgs& a, int64_t warp_base,
+                                                int (&v)[kStepsPerWarp], bool& bad) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const int64_t i = warp_base + s * 32 + lane;
+    int id = -1;
+    if (i < (int64_t)a.N) {
+      id = __ldg(a.ids + i);
+      if (id < 0 || id >= a.E) {
+        bad = true;
+        id = -1;
+      }
+    }
+    v[s] = id;
+  }
+}
+
+// ---------------------------------------------------------------- kernels
+__global__ void __launch_bounds__(kIdxThreads) idx_count_kernel(const IdxArgs a) {
+  extern __shared__ uint32_t s_cnt[];  // [E]
+  for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_cnt[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
+  int v[kStepsPerWarp];
+  bool bad = false;
+  load_warp_slots(a, warp_base, v, bad);
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    if (v[s] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[v[s]], (uint32_t)__popc(peers));
+  }
+  const int any_bad = __syncthreads_or(bad);
+  for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
+    a.counts[(int64_t)blockIdx.x * a.E + e] = s_cnt[e];
+  if (threadIdx.x == 0) a.flags[blockIdx.x] = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
+}
+
+__global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* part = smem;                      // [P][E] partial sums per block range
+  uint32_t* tot = part + kScanThreads;        // [E]
+  uint32_t* act = tot + MOE_MAX_EXPERTS;      // [E]
+  __shared__ uint32_t warp_tmp[32];
+
+  const int E = a.E, NB = a.num_blocks;
+  const int P = max(1, kScanThreads / E);
+  const int e = threadIdx.x % E, p = threadIdx.x / E;
+  const bool worker = p < P;
+  const int b0 = worker ? (int)((int64_t)NB * p / P) : 0;
+  const int b1 = worker ? (int)((int64_t)NB * (p + 1) / P) : 0;
+
+  uint32_t sum = 0;
+  for (int b = b0; b < b1; ++b) sum += a.counts[(int64_t)b * E + e];
+  if (worker) part[p * E + e] = sum;
+  __syncthreads();
+  if (threadIdx.x < E) {
+    uint32_t run = 0;
+    for (int q = 0; q < P; ++q) {
+      const uint32_t c = part[q * E + threadIdx.x];
+      part[q * E + threadIdx.x] = run;
+      run += c;
+    }
+    tot[threadIdx.x] = run;
+  }
+  __syncthreads();
+  emit_expert_table(a, tot, act, warp_tmp);
+  __syncthreads();
+  if (worker) {
+    uint32_t base = tot[e] + part[p * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const uint32_t c = a.counts[(int64_t)b * E + e];
+      a.counts[(int64_t)b * E + e] = base;
+      base += c;
+    }
+  }
+  __shared__ uint32_t s_flags;
+  if (threadIdx.x == 0) s_flags = 0;
+  __syncthreads();
+  uint32_t flags = 0;
+  for (int b = threadIdx.x; b < NB; b += kScanThreads) flags |= a.flags[b];
+  flags = __reduce_or_sync(kFullMask, flags);
+  if ((threadIdx.x & 31) == 0 && flags) atomicOr(&s_flags, flags);
+  __syncthreads();
+  if (threadIdx.x == 0) *a.status = s_flags;
+}
+
+// kFused: single CTA, N <= 2048, computes the expert table itself.
+template <bool kFused>
+__global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs a) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* s_warp = smem;                  // [kIdxWarps][E]
+  uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
+  uint32_t* s_act = s_base + a.E;           // [E] (fused only)
+  __shared__ uint32_t warp_tmp[32];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* my_cnt = s_warp + warp * a.E;
+  for (int e = lane; e < a.E; e += 32) my_cnt[e] = 0;
+  __syncwarp();
+
+  const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
+  int v[kStepsPerWarp];
+  bool bad = false;
+  load_warp_slots(a, warp_base, v, bad);
+
+  // slots of each expert in this warp
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  if constexpr (kFused) {
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+      uint32_t t = 0;
+      for (int w = 0; w < kIdxWarps; ++w) t += s_warp[w * a.E + e];
+      s_base[e] = t;
+    }
+    __syncthreads();
+    emit_expert_table(a, s_base, s_act, warp_tmp);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
+  } else {
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
+      s_base[e] = a.counts[(int64_t)blockIdx.x * a.E + e];
+  }
+  __syncthreads();
+  // per-warp running offsets: base + slots of e in earlier warps
+  for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+    uint32_t run = s_base[e];
+    for (int w = 0; w < kIdxWarps; ++w) {
+      const uint32_t c = s_warp[w * a.E + e];
+      s_warp[w * a.E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+
+  const unsigned lower = lanemask_lt();
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const int64_t i = warp_base + s * 32 + lane;
+    const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    uint32_t pos = 0xFFFFFFFFu;
+    if (v[s] >= 0) pos = my_cnt[v[s]] + (uint32_t)__popc(peers & lower);
+    __syncwarp();
+    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
+    __syncwarp();
+    if (i < (int64_t)a.N) {
+      a.restore_token_order[i] = pos;
+      if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_create_indices_workspace_size(int64_t num_slots, int32_t n_experts) {
+  if (num_slots < 0 || n_experts < 1 || n_experts > MOE_MAX_EXPERTS) return 0;
+  return moe::workspace_layout(num_slots, n_experts).total;
+}
+
+extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
+                                           uint32_t* expert_start_indices,
+                                           uint32_t* restore_token_order, int32_t* expert_ids,
+                                           uint32_t* expert_usage_stats, const int32_t* topk_ids,
+                                           int64_t num_slots, int32_t n_experts, void* workspace,
+                                           size_t workspace_bytes, uint32_t* scales_offset_p,
+                                           cudaStream_t stream) {
+  using namespace moe;
+  const int64_t N = num_slots;
+  const int E = n_experts;
+  if (N < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || N > (int64_t)0xFFFFFFFEu) return MOE_ERR_UNSUPPORTED;
+  if (scales_offset_p != nullptr) return MOE_ERR_UNSUPPORTED;
+  if (!expert_start_indices || !expert_ids || !expert_usage_stats) return MOE_ERR_NULL_PTR;
+  if (N > 0 && (!token_expert_order || !restore_token_order || !topk_ids))
+    return MOE_ERR_NULL_PTR;
+  const Layout L = workspace_layout(N, E);
+  if (!workspace || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
+  if (!aligned(token_expert_order, 4) || !aligned(expert_start_indices, 4) ||
+      !aligned(restore_token_order, 4) || !aligned(expert_ids, 4) ||
+      !aligned(expert_usage_stats, 4) || !aligned(topk_ids, 4))
+    return MOE_ERR_MISALIGNED;
+
+  char* ws = static_cast<char*>(workspace);
+  IdxArgs a;
+  a.ids = topk_ids;
+  a.token_expert_order = token_expert_order;
+  a.expert_start_indices = expert_start_indices;
+  a.restore_token_order = restore_token_order;
+  a.expert_ids = expert_ids;
+  a.stats = expert_usage_stats;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
+  a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
+  a.N = (uint32_t)N;
+  a.E = E;
+  a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);
+
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 2) * E;
+  if (L.num_blocks <= 1) {
+    idx_scatter_kernel<true><<<1, kIdxThreads, scatter_smem, stream>>>(a);
+    return launch_status();
+  }
+  idx_count_kernel<<<a.num_blocks, kIdxThreads, sizeof(uint32_t) * E, stream>>>(a);
+  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
+  idx_scan_kernel<<<1, kScanThreads, scan_smem, stream>>>(a);
+  idx_scatter_kernel<false><<<a.num_blocks, kIdxThreads, scatter_smem, stream>>>(a);
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,
+                                               cudaStream_t stream) {
+  if (!workspace || !host_status) return MOE_ERR_NULL_PTR;
+  if (cudaMemcpyAsync(host_status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

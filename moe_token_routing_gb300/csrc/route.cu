@@ -1,0 +1,394 @@
+// Group-limited top-k router for sm_103a.
+//
+// Page "group_limited_router_kernel", description paragraph: experts are split
+// into n_groups groups, the topk_group best groups are kept and the
+// n_experts_per_tok experts are chosen from them; the bias is added for the
+// selection only (Args expert_bias, expert_weights); Parameters norm_weights
+// and Args routed_scaling_factor fix the weight post-processing.
+//
+// Two kernel shapes:
+//  * E > 32: one warp per token. Lane l holds the C = E/32 (rounded up to a
+//    power of two) contiguous experts l*C .. l*C+C-1 in registers. Group
+//    scores come from a per-lane top-2 plus a butterfly over the lanes of a
+//    group; the expert top-K is K rounds of a warp-wide max (redux.sync on
+//    order-preserving integer keys) where ties resolve to the lowest lane,
+//    which holds the lowest expert index, because lanes hold ascending ranges.
+//  * E <= 32: one thread per token, all E scores in registers.
+// Both read each score row once with coalesced (vector) loads, keep the bias
+// in registers across a persistent token loop, and write K ids and weights
+// per token.
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// With at most 32 groups and C experts per lane, a group always spans at
+// least one whole lane, so two layouts cover every shape.
+enum GroupMode : int {
+  kGroupsAllKept = 0,  // topk_group == n_groups: no group selection
+  kGroupsSegment = 1,  // a group spans a power-of-two run of whole lanes
+  kGroupsGeneric = 2   // anything else: group scores through shared memory
+};
+
+struct RouteArgs {
+  int32_t* ids;
+  float* weights;
+  const float* scores;
+  const float* bias;
+  int64_t T;
+  int E, K, G, M, S;
+  int norm;
+  float scale;
+  int group_mode;
+  int seg_lanes;  // lanes per group in kGroupsSegment
+};
+
+// Running top-2 of a stream of values (multiset: equal values both count).
+__device__ __forceinline__ void top2_push(float& t1, float& t2, float x) {
+  t2 = fmaxf(t2, fminf(t1, x));
+  t1 = fmaxf(t1, x);
+}
+
+// Rank groups by (score desc, index asc) and return the bit mask of the M best.
+// Lane j < G holds g_j on entry.
+__device__ __forceinline__ uint32_t keep_best_groups(float gj, int lane, int G, int M) {
+  int ahead = 0;
+  for (int j = 0; j < G; ++j) {
+    const float gx = __shfl_sync(kFullMask, gj, j);
+    ahead += (gx > gj) || (gx == gj && j < lane);
+  }
+  return __ballot_sync(kFullMask, lane < G && ahead < M);
+}
+
+template <int C, bool kVec>
+__global__ void __launch_bounds__(kRouteThreads) route_warp_kernel(const RouteArgs a) {
+  extern __shared__ float dyn_smem[];  // kGroupsGeneric: kRouteWarps * E biased scores
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int e0 = lane * C;
+
+  float bias_r[C];
+  int grp[C];
+  bool valid[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int e = e0 + c;
+    valid[c] = e < a.E;
+    bias_r[c] = valid[c] ? a.bias[e] : 0.0f;
+    grp[c] = valid[c] ? e / a.S : 31;
+  }
+
+  const int64_t first = (int64_t)blockIdx.x * kRouteWarps + warp;
+  const int64_t stride = (int64_t)gridDim.x * kRouteWarps;
+  for (int64_t t = first; t < a.T; t += stride) {
+    const float* row = a.scores + t * a.E;
+    float s[C];
+    if constexpr (kVec) {
+#pragma unroll
+      for (int q = 0; q < C / 4; ++q) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e0 + 4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + e0 + 4 * q));
+        s[4 * q + 0] = v.x;
+        s[4 * q + 1] = v.y;
+        s[4 * q + 2] = v.z;
+        s[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] = valid[c] ? __ldg(row + e0 + c) : 0.0f;
+    }
+    float b[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) b[c] = __fadd_rn(s[c], bias_r[c]);
+
+    // ---- group selection ----
+    uint32_t kept = kFullMask;
+    if (a.group_mode == kGroupsSegment) {
+      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        if (valid[c]) top2_push(t1, t2, b[c]);
+      for (int off = 1; off < a.seg_lanes; off <<= 1) {
+        const float o1 = __shfl_xor_sync(kFullMask, t1, off);
+        const float o2 = __shfl_xor_sync(kFullMask, t2, off);
+        t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+        t1 = fmaxf(t1, o1);
+      }
+      const float g = __fadd_rn(t1, t2);
+      const float gj = __shfl_sync(kFullMask, g, lane < a.G ? lane * a.seg_lanes : 0);
+      kept = keep_best_groups(gj, lane, a.G, a.M);
+    } else if (a.group_mode == kGroupsGeneric) {
+      float* wb = dyn_smem + warp * a.E;
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        if (valid[c]) wb[e0 + c] = b[c];
+      __syncwarp();
+      float gj = 0.0f;
+      if (lane < a.G) {
+        float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+        for (int e = lane * a.S; e < (lane + 1) * a.S; ++e) top2_push(t1, t2, wb[e]);
+        gj = (a.S == 1) ? t1 : __fadd_rn(t1, t2);
+      }
+      __syncwarp();
+      kept = keep_best_groups(gj, lane, a.G, a.M);
+    }
+
+    // ---- expert top-K over the kept groups ----
+    uint32_t key[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+      key[c] = (valid[c] && ((kept >> grp[c]) & 1u)) ? ordered_key(b[c]) : 0u;
+    uint32_t head = 0;
+    int head_pos = 0;
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+      if (key[c] > head) { head = key[c]; head_pos = c; }
+
+    int my_id = 0;
+    for (int r = 0; r < a.K; ++r) {
+      const uint32_t best = __reduce_max_sync(kFullMask, head);
+      const unsigned holders = __ballot_sync(kFullMask, head == best && head != 0u);
+      const int win_lane = holders ? __ffs(holders) - 1 : 0;
+      const int id = __shfl_sync(kFullMask, e0 + head_pos, win_lane);
+      if (lane == r) my_id = id;
+      if (lane == win_lane) {
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          if (c == head_pos) key[c] = 0u;
+        head = 0;
+        head_pos = 0;
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          if (key[c] > head) { head = key[c]; head_pos = c; }
+      }
+    }
+
+    // ---- weights: unbiased score, optional normalisation, scaling ----
+    float w = (lane < a.K) ? __ldg(row + my_id) : 0.0f;
+    if (a.norm) {
+      float sum = 0.0f;
+      for (int k = 0; k < a.K; ++k) sum = __fadd_rn(sum, __shfl_sync(kFullMask, w, k));
+      w = __fdiv_rn(w, sum);
+    }
+    w = __fmul_rn(w, a.scale);
+    if (lane < a.K) {
+      a.ids[t * a.K + lane] = my_id;
+      a.weights[t * a.K + lane] = w;
+    }
+  }
+}
+
+// One thread per token, E <= EP <= 32.
+template <int EP, bool kVec>
+__global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const RouteArgs a) {
+  float bias_r[EP];
+  uint32_t valid = 0, run_start = 0, run_end = 0;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    const bool v = e < a.E;
+    bias_r[e] = v ? a.bias[e] : 0.0f;
+    valid |= (uint32_t)v << e;
+    if (v && e % a.S == 0) run_start |= 1u << e;
+    if (v && e % a.S == a.S - 1) run_end |= 1u << e;
+  }
+  const bool select_groups = a.M < a.G;
+
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < a.T; t += stride) {
+    const float* row = a.scores + t * a.E;
+    float s[EP];
+    if constexpr (kVec) {
+#pragma unroll
+      for (int q = 0; q < EP / 4; ++q) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + 4 * q));
+        s[4 * q + 0] = v.x;
+        s[4 * q + 1] = v.y;
+        s[4 * q + 2] = v.z;
+        s[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EP; ++e) s[e] = ((valid >> e) & 1u) ? __ldg(row + e) : 0.0f;
+    }
+    float b[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) b[e] = __fadd_rn(s[e], bias_r[e]);
+
+    uint32_t allowed = valid;
+    if (select_groups) {
+      // g_end[e]: top-1 + top-2 of e's group so far; g_of[e]: the whole group's score
+      float g_end[EP], g_of[EP];
+      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if ((run_start >> e) & 1u) t1 = t2 = -CUDART_INF_F;
+        top2_push(t1, t2, b[e]);
+        g_end[e] = (a.S == 1) ? t1 : __fadd_rn(t1, t2);
+      }
+      g_of[EP - 1] = g_end[EP - 1];
+#pragma unroll
+      for (int e = EP - 2; e >= 0; --e) g_of[e] = ((run_end >> e) & 1u) ? g_end[e] : g_of[e + 1];
+      // rank each group leader against the other leaders
+      uint32_t kept_leaders = 0;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if (!((run_start >> e) & 1u)) continue;
+        int ahead = 0;
+#pragma unroll
+        for (int f = 0; f < EP; ++f) {
+          if (!((run_start >> f) & 1u)) continue;
+          ahead += (g_of[f] > g_of[e]) || (g_of[f] == g_of[e] && f < e);
+        }
+        if (ahead < a.M) kept_leaders |= 1u << e;
+      }
+      allowed = 0;
+      bool keep = false;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if ((run_start >> e) & 1u) keep = (kept_leaders >> e) & 1u;
+        if (keep && ((valid >> e) & 1u)) allowed |= 1u << e;
+      }
+    }
+
+    uint32_t key[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) key[e] = ((allowed >> e) & 1u) ? ordered_key(b[e]) : 0u;
+
+    float sum = 0.0f;
+    int32_t* ids_row = a.ids + t * a.K;
+    float* w_row = a.weights + t * a.K;
+    for (int r = 0; r < a.K; ++r) {
+      uint32_t best = 0;
+      int best_e = 0;
+      float best_s = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (key[e] > best) { best = key[e]; best_e = e; best_s = s[e]; }
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e == best_e) key[e] = 0u;
+      ids_row[r] = best_e;
+      w_row[r] = best_s;
+      sum = __fadd_rn(sum, best_s);
+    }
+    for (int r = 0; r < a.K; ++r) {
+      float w = w_row[r];
+      if (a.norm) w = __fdiv_rn(w, sum);
+      w_row[r] = __fmul_rn(w, a.scale);
+    }
+  }
+}
+
+template <typename Kernel>
+int ctas_per_sm(Kernel k, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRouteThreads, smem) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  return n;
+}
+
+template <typename Kernel>
+moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, size_t smem,
+                          cudaStream_t stream) {
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  const int64_t want = (a.T + tokens_per_cta - 1) / tokens_per_cta;
+  const int64_t cap = (int64_t)device_info().sm_count * ctas_per_sm(k, smem);
+  const int grid = (int)(want < cap ? want : cap);
+  k<<<grid, kRouteThreads, smem, stream>>>(a);
+  return launch_status();
+}
+
+template <int C>
+moe_status_t launch_warp_path(const RouteArgs& a, bool vec, cudaStream_t stream) {
+  const size_t smem =
+      a.group_mode == kGroupsGeneric ? (size_t)kRouteWarps * a.E * sizeof(float) : 0;
+  if constexpr (C % 4 == 0) {
+    if (vec) return launch_route(route_warp_kernel<C, true>, a, kRouteWarps, smem, stream);
+  }
+  return launch_route(route_warp_kernel<C, false>, a, kRouteWarps, smem, stream);
+}
+
+template <int EP>
+moe_status_t launch_thread_path(const RouteArgs& a, bool vec, cudaStream_t stream) {
+  if (vec) return launch_route(route_thread_kernel<EP, true>, a, kRouteThreads, 0, stream);
+  return launch_route(route_thread_kernel<EP, false>, a, kRouteThreads, 0, stream);
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
+                                  const float* expert_scores, const float* expert_bias,
+                                  int64_t num_tokens, int32_t n_routed_experts,
+                                  int32_t n_experts_per_tok, int32_t n_groups,
+                                  int32_t topk_group, int32_t norm_weights,
+                                  float routed_scaling_factor, cudaStream_t stream) {
+  using namespace moe;
+  const int E = n_routed_experts, K = n_experts_per_tok, G = n_groups, M = topk_group;
+  if (num_tokens < 0 || E < 1 || G < 1 || M < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (E % G != 0 || M > G) return MOE_ERR_INVALID_ARG;
+  const int S = E / G;
+  if ((int64_t)K > (int64_t)M * S) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || G > MOE_MAX_GROUPS || K > MOE_MAX_EXPERTS_PER_TOK)
+    return MOE_ERR_UNSUPPORTED;
+  if (num_tokens > (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MOE_OK;
+  if (!expert_indices || !expert_weights || !expert_scores || !expert_bias)
+    return MOE_ERR_NULL_PTR;
+  if (!aligned(expert_indices, 4) || !aligned(expert_weights, 4) || !aligned(expert_scores, 4) ||
+      !aligned(expert_bias, 4))
+    return MOE_ERR_MISALIGNED;
+
+  RouteArgs a;
+  a.ids = expert_indices;
+  a.weights = expert_weights;
+  a.scores = expert_scores;
+  a.bias = expert_bias;
+  a.T = num_tokens;
+  a.E = E;
+  a.K = K;
+  a.G = G;
+  a.M = M;
+  a.S = S;
+  a.norm = norm_weights != 0;
+  a.scale = routed_scaling_factor;
+  a.group_mode = kGroupsAllKept;
+  a.seg_lanes = 1;
+  const bool vec = (E % 4 == 0) && aligned(expert_scores, 16);
+
+  if (E <= 32) {
+    if (E <= 8) return launch_thread_path<8>(a, vec, stream);
+    if (E <= 16) return launch_thread_path<16>(a, vec, stream);
+    return launch_thread_path<32>(a, vec, stream);
+  }
+  const int C = E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
+  if (M < G) {
+    if (S % C == 0 && is_pow2(S / C)) {
+      a.group_mode = kGroupsSegment;
+      a.seg_lanes = S / C;
+    } else {
+      a.group_mode = kGroupsGeneric;
+    }
+  }
+  switch (C) {
+    case 2: return launch_warp_path<2>(a, vec, stream);
+    case 4: return launch_warp_path<4>(a, vec, stream);
+    case 8: return launch_warp_path<8>(a, vec, stream);
+    case 16: return launch_warp_path<16>(a, vec, stream);
+    default: return launch_warp_path<32>(a, vec, stream);
+  }
+}

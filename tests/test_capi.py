@@ -1,0 +1,116 @@
+"""The C ABI library without a GPU: it loads, exports every entry point that
+include/moe_routing.h declares, and rejects bad arguments on the host before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_routing.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_token_routing_gb300 import build
+    build.build()
+    import moe_token_routing_gb300 as moe
+    return moe.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(
+        ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
+         "moe_create_indices", "moe_finalize", "moe_read_device_status"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import moe_token_routing_gb300 as moe
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(moe.EXPORTED_SYMBOLS) == declared_functions()
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(6) == b"MOE_ERR_WORKSPACE"
+    assert lib.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+def test_workspace_size_query(lib):
+    assert lib.moe_create_indices_workspace_size(0, 8) == 256
+    assert lib.moe_create_indices_workspace_size(2048, 8) == 256
+    big = lib.moe_create_indices_workspace_size(131072, 256)
+    assert big >= 64 * 256 * 4 and big % 256 == 0
+    assert lib.moe_create_indices_workspace_size(-1, 8) == 0
+    assert lib.moe_create_indices_workspace_size(10, 0) == 0
+    assert lib.moe_create_indices_workspace_size(10, 1025) == 0
+
+
+FAKE = 0x7f0000001000  # never dereferenced: every call below fails host validation
+
+
+def test_route_host_validation(lib):
+    f = lib.moe_route
+    ok = (FAKE, FAKE, FAKE, FAKE)
+    assert f(*ok, 4, 256, 8, 7, 4, 1, 1.0, None) == 2      # E % n_groups
+    assert f(*ok, 4, 256, 8, 8, 9, 1, 1.0, None) == 2      # topk_group > n_groups
+    assert f(*ok, 4, 256, 0, 8, 4, 1, 1.0, None) == 2      # K < 1
+    assert f(*ok, 4, 16, 5, 4, 1, 1, 1.0, None) == 2       # K > topk_group * group size
+    assert f(*ok, -1, 256, 8, 8, 4, 1, 1.0, None) == 2     # T < 0
+    assert f(*ok, 4, 2048, 8, 8, 4, 1, 1.0, None) == 4     # E above the limit
+    assert f(*ok, 4, 256, 8, 64, 4, 1, 1.0, None) == 4     # n_groups above the limit
+    assert f(None, FAKE, FAKE, FAKE, 4, 256, 8, 8, 4, 1, 1.0, None) == 1
+    assert f(FAKE + 2, FAKE, FAKE, FAKE, 4, 256, 8, 8, 4, 1, 1.0, None) == 3
+    assert f(None, None, None, None, 0, 256, 8, 8, 4, 1, 1.0, None) == 0  # T = 0: nothing to do
+
+
+def test_create_indices_host_validation(lib):
+    f = lib.moe_create_indices
+    outs = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    ws = lib.moe_create_indices_workspace_size(100000, 64)
+    assert f(*outs, 100000, 64, FAKE, ws, FAKE, None) == 4          # scales_offset_p given
+    assert f(*outs, 100000, 64, FAKE, ws - 1, None, None) == 6      # workspace too small
+    assert f(*outs, 100000, 64, None, ws, None, None) == 6          # no workspace
+    assert f(*outs, 100000, 64, FAKE + 16, ws, None, None) == 3     # workspace alignment
+    assert f(*outs, -1, 64, FAKE, ws, None, None) == 2
+    assert f(*outs, 10, 0, FAKE, ws, None, None) == 2
+    assert f(*outs, 10, 2000, FAKE, ws, None, None) == 4
+    assert f(FAKE, None, FAKE, FAKE, FAKE, FAKE, 10, 64, FAKE, ws, None, None) == 1
+    assert f(FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE, 10, 64, FAKE, ws, None, None) == 3
+
+
+def test_finalize_host_validation(lib):
+    f = lib.moe_finalize
+    p = (FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000)
+    assert f(*p, 4, 2, 60, None) == 4          # hidden % 8
+    assert f(*p, 4, 0, 64, None) == 2
+    assert f(*p, 4, 33, 64, None) == 4
+    assert f(*p, -1, 2, 64, None) == 2
+    assert f(None, *p[1:], 4, 2, 64, None) == 1
+    assert f(p[0] + 8, *p[1:], 4, 2, 64, None) == 3
+    assert f(p[0], p[0], p[2], p[3], 4, 2, 64, None) == 2   # output overlaps down
+    assert f(None, None, None, None, 0, 2, 64, None) == 0   # T = 0
+
+
+def test_device_status_host_validation(lib):
+    out = ctypes.c_uint32(0)
+    assert lib.moe_read_device_status(None, ctypes.byref(out), None) == 1
+    assert lib.moe_read_device_status(FAKE, None, None) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import moe_token_routing_gb300 as moe
+    s = torch.rand(4, 16)
+    with pytest.raises(ValueError):
+        moe.route(s, torch.zeros(16), 2, 4, 2, True, 1.0)

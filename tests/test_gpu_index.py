@@ -1,0 +1,111 @@
+"""GPU parity of moe_create_indices (moe_create_indices page) against the oracle.
+
+Every output is integer data and must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _workloads import workload
+from test_oracle_index import check_index_outputs
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("token_expert_order", "expert_start_indices", "restore_token_order", "expert_ids",
+        "expert_usage_stats")
+
+
+def gpu_index(ids, E):
+    import moe_token_routing_gb300 as moe
+    t = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)).cuda()
+    bufs = moe.create_indices(t, E)
+    torch.cuda.synchronize()
+    out = {k: getattr(bufs, k).cpu().numpy() for k in KEYS}
+    for k in ("token_expert_order", "expert_start_indices", "restore_token_order",
+              "expert_usage_stats"):
+        out[k] = out[k].view(np.uint32)
+    return out, bufs.device_status()
+
+
+def assert_index_parity(ids, E):
+    ref = oracle.create_indices(ids, E)
+    got, status = gpu_index(ids, E)
+    assert status == 0
+    for k in KEYS:
+        assert np.array_equal(got[k], ref[k]), k
+    return got
+
+
+@pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
+def test_parity_on_workloads(name):
+    cfg, _, _, ids, _, ref = workload(name)
+    got, status = gpu_index(ids, cfg.E)
+    assert status == 0
+    for k in KEYS:
+        assert np.array_equal(got[k], ref[k]), k
+
+
+@pytest.mark.parametrize("N", [0, 1, 31, 2047, 2048, 2049, 4113, 100003])
+@pytest.mark.parametrize("E", [1, 3, 8, 64, 256, 1000, 1024])
+def test_random_ids(N, E):
+    rng = np.random.default_rng(N * 31 + E)
+    ids = rng.integers(0, E, size=N).astype(np.int32)
+    got = assert_index_parity(ids, E)
+    check_index_outputs(ids, E, got)
+
+
+def test_all_slots_on_one_expert_past_any_cache():
+    ids = np.full(300001, 5, dtype=np.int32)
+    got = assert_index_parity(ids, 64)
+    assert got["expert_usage_stats"].tolist() == [300001, 1]
+
+
+def test_hot_experts_and_idle_experts():
+    """Eight hot experts far past 8192 slots each, most experts idle."""
+    rng = np.random.default_rng(4)
+    ids = rng.integers(0, 8, size=262144).astype(np.int32)
+    ids[::97] = 100
+    assert_index_parity(ids, 128)
+
+
+def test_every_expert_active_descending():
+    E = 1024
+    ids = np.tile(np.arange(E, dtype=np.int32)[::-1], 37)
+    assert_index_parity(ids, E)
+
+
+def test_bad_expert_id_flagged():
+    import moe_token_routing_gb300 as moe
+    for N in (100, 10000):
+        ids = np.zeros(N, dtype=np.int32)
+        ids[N // 2] = 64  # out of range for E = 64
+        ids[N // 3] = -3
+        t = torch.from_numpy(ids).cuda()
+        bufs = moe.create_indices(t, 64)
+        assert bufs.device_status() & moe.DEVICE_STATUS_BAD_EXPERT_ID
+        # a clean call on the same workspace clears the flag
+        bufs.run(torch.zeros(N, dtype=torch.int32, device="cuda"))
+        assert bufs.device_status() == 0
+
+
+def test_workspace_checks():
+    import moe_token_routing_gb300 as moe
+    N, E = 10000, 64
+    need = moe.moe_create_indices_workspace_size(N, E)
+    assert need >= 256
+    bufs = moe.IndexBuffers(N, E, "cuda")
+    bufs.workspace = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    ids = torch.zeros(N, dtype=torch.int32, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        bufs.run(ids)
+    assert ei.value.status == 6
+
+
+def test_deterministic():
+    cfg, _, _, ids, _, _ = workload("dsv3_prefill")
+    a, _ = gpu_index(ids, cfg.E)
+    b, _ = gpu_index(ids, cfg.E)
+    for k in KEYS:
+        assert np.array_equal(a[k], b[k])

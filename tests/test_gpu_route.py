@@ -1,0 +1,149 @@
+"""GPU parity of moe_route (group_limited_router_kernel page) against the oracle.
+
+Expert ids must be bit-exact; weights within 1e-6 relative error (fp32).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _workloads import workload
+
+pytestmark = pytest.mark.gpu
+
+CONFIG_NAMES = [c.name for c in synth.CONFIGS]
+
+
+def _moe():
+    import moe_token_routing_gb300 as moe
+    moe.load_library()
+    return moe
+
+
+def gpu_route(scores, bias, K, G, M, norm, scale, scores_offset=0):
+    moe = _moe()
+    s = torch.from_numpy(np.ascontiguousarray(scores)).cuda()
+    if scores_offset:
+        # same values at a pointer that is only 4-byte aligned (scalar-load path)
+        buf = torch.empty(s.numel() + scores_offset, dtype=torch.float32, device="cuda")
+        buf[scores_offset:] = s.reshape(-1)
+        s = buf[scores_offset:].view(s.shape)
+    b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
+    ids, w = moe.route(s, b, K, G, M, norm, scale)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+def assert_route_parity(scores, bias, K, G, M, norm, scale, **kw):
+    ids_ref, w_ref = oracle.route(scores, bias, K, G, M, norm, scale)
+    ids, w = gpu_route(scores, bias, K, G, M, norm, scale, **kw)
+    bad = np.nonzero((ids != ids_ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first token {bad[:1]}: {ids[bad[:1]]} vs {ids_ref[bad[:1]]}"
+    np.testing.assert_allclose(w, w_ref, rtol=1e-6, atol=0)
+    return ids, w
+
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_parity_on_workloads(name):
+    cfg, scores, bias, ids_ref, w_ref, _ = workload(name)
+    ids, w = gpu_route(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    assert np.array_equal(ids, ids_ref)
+    np.testing.assert_allclose(w, w_ref, rtol=1e-6, atol=0)
+    # same arithmetic in the same order: expected bit-identical
+    assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
+# (E, G, M, K): thread-per-token path (E <= 32) and the warp path's group layouts
+SHAPES = [
+    (8, 1, 1, 2), (8, 4, 2, 3), (12, 3, 2, 4), (16, 4, 2, 4), (16, 16, 5, 5), (24, 8, 3, 6),
+    (32, 4, 2, 8), (32, 32, 7, 7),
+    (48, 4, 2, 6), (64, 8, 4, 8), (64, 32, 8, 8), (64, 1, 1, 6), (96, 4, 2, 8),
+    (128, 8, 4, 8), (128, 32, 4, 8), (128, 1, 1, 8), (160, 8, 3, 6), (192, 6, 3, 8),
+    (256, 8, 4, 8), (256, 16, 4, 8), (256, 32, 8, 16), (256, 2, 1, 8), (256, 4, 1, 8),
+    (256, 1, 1, 32), (384, 1, 1, 8), (384, 12, 4, 8), (512, 8, 2, 16), (1024, 32, 4, 8),
+]
+
+
+@pytest.mark.parametrize("E,G,M,K", SHAPES)
+@pytest.mark.parametrize("norm", [True, False])
+def test_parity_shapes(E, G, M, K, norm):
+    rng = np.random.default_rng(E * 7919 + G * 31 + M * 7 + K)
+    T = 333
+    scores = rng.random((T, E), dtype=np.float32)
+    bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    assert_route_parity(scores, bias, K, G, M, norm, 1.5)
+
+
+@pytest.mark.parametrize("E,G,M,K", [(16, 4, 2, 4), (128, 8, 4, 8), (256, 8, 4, 8),
+                                     (160, 8, 3, 6), (64, 32, 8, 8)])
+def test_tie_stress(E, G, M, K):
+    """Scores on a 1/8 grid: many equal biased scores, group scores and ranks."""
+    rng = np.random.default_rng(E + K)
+    T = 512
+    scores = (rng.integers(0, 9, size=(T, E)) / 8).astype(np.float32)
+    for bias in (np.zeros(E, np.float32), np.full(E, 0.125, np.float32),
+                 (rng.integers(-1, 2, size=E) / 8).astype(np.float32)):
+        assert_route_parity(scores, bias, K, G, M, True, 1.0)
+
+
+def test_all_equal_and_signed_zero():
+    E, G, M, K = 256, 8, 4, 8
+    scores = np.zeros((64, E), dtype=np.float32)
+    scores[1::2] = -0.0
+    bias = np.zeros(E, np.float32)
+    bias[::3] = -0.0
+    ids, _ = assert_route_parity(scores, bias, K, G, M, False, 1.0)
+    assert (ids == np.arange(K)).all()
+
+
+@pytest.mark.parametrize("E", [16, 256])
+def test_unaligned_scores_use_scalar_loads(E):
+    rng = np.random.default_rng(11)
+    scores = rng.random((77, E), dtype=np.float32)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    G = 4 if E == 16 else 8
+    assert_route_parity(scores, bias, 4, G, 2, True, 2.0, scores_offset=1)
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 255, 257, 4097, 100000])
+def test_token_counts(T):
+    E, G, M, K = 256, 8, 4, 8
+    cfg = synth.get_config("dsv3_prefill")
+    scores = synth.make_scores(cfg, n_tokens=T)
+    bias = synth.make_bias(cfg)
+    assert_route_parity(scores, bias, K, G, M, True, 2.5)
+
+
+def test_zero_tokens_is_noop():
+    moe = _moe()
+    ids = torch.full((0, 8), -7, dtype=torch.int32, device="cuda")
+    w = torch.empty((0, 8), dtype=torch.float32, device="cuda")
+    s = torch.empty((0, 256), dtype=torch.float32, device="cuda")
+    b = torch.zeros(256, dtype=torch.float32, device="cuda")
+    moe.moe_route(ids, w, s, b, 8, 4, True, 1.0)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("E,G,M,K,status", [(256, 7, 4, 8, 2), (256, 8, 9, 8, 2),
+                                            (256, 8, 1, 33, 2), (256, 8, 4, 0, 2),
+                                            (2048, 8, 4, 8, 4), (256, 8, 4, 33, 4),
+                                            (32, 32, 1, 2, 2)])
+def test_invalid_arguments(E, G, M, K, status):
+    moe = _moe()
+    T = 4
+    s = torch.rand((T, E), device="cuda")
+    b = torch.zeros(E, device="cuda")
+    ids = torch.empty((T, max(K, 1)), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, max(K, 1)), dtype=torch.float32, device="cuda")
+    lib = moe.load_library()
+    rc = lib.moe_route(ids.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), T, E, K, G, M, 1,
+                       1.0, torch.cuda.current_stream().cuda_stream)
+    assert rc == status
+
+
+def test_deterministic():
+    cfg, scores, bias, *_ = workload("dsv3_prefill")
+    a = gpu_route(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    b = gpu_route(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
