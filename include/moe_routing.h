@@ -166,6 +166,47 @@ moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
 moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,
                                     cudaStream_t stream);
 
+/*
+ * moe_create_indices_no_alloc -- the same index build as moe_create_indices,
+ * for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point.
+ *
+ * Why: some callers can hand a kernel only the tensors it declares as inputs
+ * and outputs. One example is an operator inside a framework whose memory
+ * pool owns all device memory and offers no scratch request. Another is a
+ * serving loop that reserves memory at start-up and must not call cudaMalloc
+ * on the request path. Such callers cannot provide moe_create_indices'
+ * workspace. This variant keeps its scratch in a file-scope __device__
+ * array of MOE_NO_ALLOC_SCRATCH_BYTES bytes inside the library. Every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ * Outputs, inputs and their requirements are those of moe_create_indices.
+ * device_status: optional device pointer (4-byte aligned, or NULL) that
+ *   receives the device status word (MOE_DEVICE_STATUS_* bits, 0 = clean).
+ *   When it is NULL the word is written inside the scratch and cannot be read.
+ * Limits: the scratch that moe_create_indices_workspace_size(num_slots,
+ *   n_experts) reports must fit in MOE_NO_ALLOC_SCRATCH_BYTES; a larger
+ *   request returns MOE_ERR_WORKSPACE before anything is enqueued. With 1 MiB
+ *   this covers, for example, 2 million slots over 128 experts or 1 million
+ *   slots over 256 experts.
+ * Allocation: the call makes no cudaMalloc, cudaFree or other allocating
+ *   call. The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it, so make that first call before
+ *   any stream capture begins.
+ * Sharing: all calls on a device use the same array. Calls whose work
+ *   overlaps on the GPU (different streams, no ordering between them) race on
+ *   it and give wrong results. Calls ordered one after another are safe.
+ *   No scratch word needs clearing between calls: each call writes every
+ *   word it reads before reading it.
+ */
+#define MOE_NO_ALLOC_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order,
+                                         uint32_t* expert_start_indices,
+                                         uint32_t* restore_token_order, int32_t* expert_ids,
+                                         uint32_t* expert_usage_stats, const int32_t* topk_ids,
+                                         int64_t num_slots, int32_t n_experts,
+                                         uint32_t* device_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,8 @@ DEVICE_STATUS_BAD_EXPERT_ID = 0x1
 
 # Entry points declared in include/moe_routing.h.
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
-                    "moe_create_indices", "moe_finalize", "moe_read_device_status")
+                    "moe_create_indices", "moe_finalize", "moe_read_device_status",
+                    "moe_create_indices_no_alloc")
 
 
 class MoeError(RuntimeError):
@@ -158,6 +159,34 @@ def moe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
                                                ctypes.byref(out), _stream(stream))
     _check("moe_read_device_status", rc)
     return int(out.value)
+
+
+def moe_create_indices_no_alloc(token_expert_order: torch.Tensor,
+                                expert_start_indices: torch.Tensor,
+                                restore_token_order: torch.Tensor, expert_ids: torch.Tensor,
+                                expert_usage_stats: torch.Tensor, topk_ids: torch.Tensor,
+                                device_status: torch.Tensor | None = None, stream=None) -> None:
+    """moe_create_indices without a workspace, for callers that cannot allocate
+    device memory: the library's own static scratch array is used instead
+    (see include/moe_routing.h for its size limit and sharing rules).
+    device_status, if given, is a 1-element int32 CUDA tensor that receives
+    the device status word."""
+    lib = load_library()
+    f = lib.moe_create_indices_no_alloc
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
+    f.restype = ctypes.c_int
+    N = topk_ids.numel()
+    E = expert_ids.numel()
+    args = (_dev(token_expert_order, "token_expert_order", torch.int32, (N,)),
+            _dev(expert_start_indices, "expert_start_indices", torch.int32, (E + 1,)),
+            _dev(restore_token_order, "restore_token_order", torch.int32, (N,)),
+            _dev(expert_ids, "expert_ids", torch.int32, (E,)),
+            _dev(expert_usage_stats, "expert_usage_stats", torch.int32, (2,)),
+            _dev(topk_ids.reshape(-1), "topk_ids", torch.int32))
+    status = None if device_status is None else _dev(device_status, "device_status",
+                                                     torch.int32, (1,))
+    _check("moe_create_indices_no_alloc", f(*args, N, E, status, _stream(stream)))
 
 
 # ---------------------------------------------------------------- allocating helpers

@@ -20,6 +20,8 @@
 //             (lower lanes of its step with the same e). Writes
 //             token_expert_order and restore_token_order in one pass.
 //   For N <= 2048 one CTA does all three in one launch.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -378,4 +380,92 @@ extern "C" moe_status_t moe_read_device_status(const void* workspace, uint32_t* 
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch of moe_create_indices_no_alloc: one array per device, created when
+// the library is loaded and kept until the process exits. Host code may not
+// use the name as an address (on the host it names a stand-in object); the
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[MOE_NO_ALLOC_SCRATCH_BYTES];
+
+namespace moe {
+namespace {
+
+// Device address of g_no_alloc_scratch on the current device, looked up on
+// the first call made on that device and cached.
+moe_status_t no_alloc_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order,
+                                                    uint32_t* expert_start_indices,
+                                                    uint32_t* restore_token_order,
+                                                    int32_t* expert_ids,
+                                                    uint32_t* expert_usage_stats,
+                                                    const int32_t* topk_ids, int64_t num_slots,
+                                                    int32_t n_experts, uint32_t* device_status,
+                                                    cudaStream_t stream) {
+  using namespace moe;
+  const int64_t N = num_slots;
+  const int E = n_experts;
+  if (N < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || N > (int64_t)0xFFFFFFFEu) return MOE_ERR_UNSUPPORTED;
+  if (!expert_start_indices || !expert_ids || !expert_usage_stats) return MOE_ERR_NULL_PTR;
+  if (N > 0 && (!token_expert_order || !restore_token_order || !topk_ids))
+    return MOE_ERR_NULL_PTR;
+  const Layout L = workspace_layout(N, E);
+  if (L.total > (size_t)MOE_NO_ALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  if (!aligned(token_expert_order, 4) || !aligned(expert_start_indices, 4) ||
+      !aligned(restore_token_order, 4) || !aligned(expert_ids, 4) ||
+      !aligned(expert_usage_stats, 4) || !aligned(topk_ids, 4) || !aligned(device_status, 4))
+    return MOE_ERR_MISALIGNED;
+
+  void* scratch = nullptr;
+  const moe_status_t st = no_alloc_scratch_address(&scratch);
+  if (st != MOE_OK) return st;
+
+  // Every scratch word that a kernel reads is written earlier in the same
+  // call, so nothing has to be cleared between calls.
+  char* ws = static_cast<char*>(scratch);
+  IdxArgs a;
+  a.ids = topk_ids;
+  a.token_expert_order = token_expert_order;
+  a.expert_start_indices = expert_start_indices;
+  a.restore_token_order = restore_token_order;
+  a.expert_ids = expert_ids;
+  a.stats = expert_usage_stats;
+  a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(ws);
+  a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
+  a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
+  a.N = (uint32_t)N;
+  a.E = E;
+  a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);
+
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 2) * E;
+  if (L.num_blocks <= 1) {
+    idx_scatter_kernel<true><<<1, kIdxThreads, scatter_smem, stream>>>(a);
+    return launch_status();
+  }
+  idx_count_kernel<<<a.num_blocks, kIdxThreads, sizeof(uint32_t) * E, stream>>>(a);
+  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
+  idx_scan_kernel<<<1, kScanThreads, scan_smem, stream>>>(a);
+  idx_scatter_kernel<false><<<a.num_blocks, kIdxThreads, scatter_smem, stream>>>(a);
+  return launch_status();
 }

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
-         "moe_create_indices", "moe_finalize", "moe_read_device_status"])
+         "moe_create_indices", "moe_finalize", "moe_read_device_status",
+         "moe_create_indices_no_alloc"])
 
 
 def test_every_declared_symbol_is_exported(lib):
