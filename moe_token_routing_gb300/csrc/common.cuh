@@ -37,4 +37,35 @@ inline moe_status_t launch_status() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Every kernel of the library starts with this: with programmatic dependent
+// launch the grid may begin while the previous kernel on the stream is still
+// finishing, and this waits until that kernel has completed and its writes are
+// visible. Without programmatic launch it returns at once.
+__device__ __forceinline__ void wait_for_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches `kernel` on `stream` with programmatic stream serialisation, so its
+// launch overlaps the tail of the preceding kernel (which it then waits for in
+// wait_for_prior_grid).
+template <typename... KArgs, typename... Args>
+moe_status_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 }  // namespace moe

@@ -10,16 +10,20 @@
 //
 // Design (no inter-CTA waits, deterministic, stable):
 //   count   : CTA b counts the experts of its 2048 slots (warp-aggregated with
-//             match.any, shared-memory counters) -> counts[b][e].
-//   scan    : one CTA turns counts into bases: base[b][e] = start(e) +
-//             sum_{b' < b} counts[b'][e], and writes the compact CSR,
-//             expert_ids, usage stats and the device status word.
-//   scatter : CTA b re-reads its slots; within a CTA each warp owns 256
+//             match.any, shared-memory counters) -> counts[e][b] (expert-major,
+//             so one expert's counts are contiguous).
+//   scatter : CTA b derives its bases itself from the small count matrix:
+//             base[b][e] = start(e) + sum_{b' < b} counts[e][b'], with start(e)
+//             the exclusive sum of the per-expert totals; CTA 0 also writes the
+//             compact CSR, expert_ids, usage stats and the device status word.
+//             Then it re-reads its slots; within a CTA each warp owns 256
 //             consecutive slots, so a slot's position is base[b][e] + (slots of
 //             e in earlier warps) + (slots of e in earlier steps of its warp) +
 //             (lower lanes of its step with the same e). Writes
 //             token_expert_order and restore_token_order in one pass.
-//   For N <= 2048 one CTA does all three in one launch.
+//   For N <= 2048 one CTA does everything in one launch. When the count matrix
+//   is too large for every CTA to read it (more than 32Ki words), a one-CTA
+//   scan kernel turns the counts into bases in between.
 #include <mutex>
 
 #include "common.cuh"
@@ -37,21 +41,25 @@ constexpr size_t kHeaderBytes = 256;
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+constexpr int64_t kMaxSharedCountWords = 32 * 1024;  // every scatter CTA reads them all
+
 struct Layout {
   int64_t num_blocks;
+  int64_t row;  // words per expert row of the count matrix (num_blocks rounded up to 4)
   size_t flags_off, counts_off, total;
 };
 
 Layout workspace_layout(int64_t N, int E) {
   Layout L;
   L.num_blocks = (N + kSlotsPerCta - 1) / kSlotsPerCta;
+  L.row = (L.num_blocks + 3) & ~(int64_t)3;
   L.flags_off = kHeaderBytes;
   if (L.num_blocks <= 1) {
     L.counts_off = kHeaderBytes;
     L.total = kHeaderBytes;
   } else {
     L.counts_off = L.flags_off + align256(sizeof(uint32_t) * (size_t)L.num_blocks);
-    L.total = L.counts_off + align256(sizeof(uint32_t) * (size_t)L.num_blocks * (size_t)E);
+    L.total = L.counts_off + align256(sizeof(uint32_t) * (size_t)L.row * (size_t)E);
   }
   return L;
 }
@@ -65,10 +73,11 @@ struct IdxArgs {
   uint32_t* stats;
   uint32_t* status;  // workspace word 0
   uint32_t* flags;   // [num_blocks]
-  uint32_t* counts;  // [num_blocks][E], overwritten with bases by the scan
+  uint32_t* counts;  // [E][row]; the scan kernel, when used, overwrites it with bases
   uint32_t N;
   int E;
   int num_blocks;
+  int row;
 };
 
 // ---------------------------------------------------------------- block helpers
@@ -126,7 +135,7 @@ __device__ uint32_t block_max(uint32_t v, uint32_t* warp_tmp) {
 // expert_ids and usage stats, and turns tot[] into each expert's start offset.
 // `act` is E words of shared scratch.
 __device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act,
-                                  uint32_t* warp_tmp) {
+                                  uint32_t* warp_tmp, bool write = true) {
   uint32_t local_max = 0;
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
     act[e] = tot[e] > 0u;
@@ -136,6 +145,7 @@ __device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act
   const uint32_t max_count = block_max(local_max, warp_tmp);
   const uint32_t active = block_exclusive_scan(act, a.E, warp_tmp);
   block_exclusive_scan(tot, a.E, warp_tmp);  // tot[e] := start of expert e
+  if (!write) return;
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
     const bool is_active = (e + 1 < a.E ? act[e + 1] : active) != act[e];
     if (is_active) {
@@ -175,6 +185,7 @@ __device__ __forceinline__ void load_warp_slots(const IdxArgs& a, int64_t warp_b
 // ---------------------------------------------------------------- kernels
 __global__ void __launch_bounds__(kIdxThreads) idx_count_kernel(const IdxArgs a) {
   extern __shared__ uint32_t s_cnt[];  // [E]
+  wait_for_prior_grid();
   for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_cnt[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -189,7 +200,12 @@ __global__ void __launch_bounds__(kIdxThreads) idx_count_kernel(const IdxArgs a)
   }
   const int any_bad = __syncthreads_or(bad);
   for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
-    a.counts[(int64_t)blockIdx.x * a.E + e] = s_cnt[e];
+    a.counts[(int64_t)e * a.row + blockIdx.x] = s_cnt[e];
+  if (blockIdx.x == a.num_blocks - 1) {  // padding columns of the count rows
+    const int pad = a.row - a.num_blocks;
+    for (int j = threadIdx.x; j < a.E * pad; j += kIdxThreads)
+      a.counts[(int64_t)(j / pad) * a.row + a.num_blocks + j % pad] = 0u;
+  }
   if (threadIdx.x == 0) a.flags[blockIdx.x] = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
 }
 
@@ -199,6 +215,7 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
   uint32_t* tot = part + kScanThreads;        // [E]
   uint32_t* act = tot + MOE_MAX_EXPERTS;      // [E]
   __shared__ uint32_t warp_tmp[32];
+  wait_for_prior_grid();
 
   const int E = a.E, NB = a.num_blocks;
   const int P = max(1, kScanThreads / E);
@@ -208,7 +225,8 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
   const int b1 = worker ? (int)((int64_t)NB * (p + 1) / P) : 0;
 
   uint32_t sum = 0;
-  for (int b = b0; b < b1; ++b) sum += a.counts[(int64_t)b * E + e];
+#pragma unroll 8
+  for (int b = b0; b < b1; ++b) sum += a.counts[(int64_t)e * a.row + b];
   if (worker) part[p * E + e] = sum;
   __syncthreads();
   if (threadIdx.x < E) {
@@ -226,8 +244,8 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
   if (worker) {
     uint32_t base = tot[e] + part[p * E + e];
     for (int b = b0; b < b1; ++b) {
-      const uint32_t c = a.counts[(int64_t)b * E + e];
-      a.counts[(int64_t)b * E + e] = base;
+      const uint32_t c = a.counts[(int64_t)e * a.row + b];
+      a.counts[(int64_t)e * a.row + b] = base;
       base += c;
     }
   }
@@ -242,14 +260,23 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
   if (threadIdx.x == 0) *a.status = s_flags;
 }
 
-// kFused: single CTA, N <= 2048, computes the expert table itself.
-template <bool kFused>
+// Where a scatter CTA takes its per-expert bases from.
+enum BaseSource : int {
+  kBasesSingleCta = 0,  // one CTA covers all slots: the bases are the expert starts
+  kBasesFromCounts = 1, // each CTA sums the count matrix itself
+  kBasesFromScan = 2    // the scan kernel wrote them into the count matrix
+};
+
+template <int kBases>
 __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs a) {
   extern __shared__ uint32_t smem[];
-  uint32_t* s_warp = smem;                  // [kIdxWarps][E]
+  uint32_t* s_warp = smem;                      // [kIdxWarps][E]
   uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
-  uint32_t* s_act = s_base + a.E;           // [E] (fused only)
+  uint32_t* s_act = s_base + a.E;               // [E]
+  uint32_t* s_pre = s_act + a.E;                // [E]
   __shared__ uint32_t warp_tmp[32];
+  __shared__ uint32_t s_flags;
+  wait_for_prior_grid();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* my_cnt = s_warp + warp * a.E;
@@ -270,7 +297,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   }
   __syncthreads();
 
-  if constexpr (kFused) {
+  if constexpr (kBases == kBasesSingleCta) {
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
       uint32_t t = 0;
       for (int w = 0; w < kIdxWarps; ++w) t += s_warp[w * a.E + e];
@@ -280,9 +307,37 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     emit_expert_table(a, s_base, s_act, warp_tmp);
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
+  } else if constexpr (kBases == kBasesFromCounts) {
+    // totals and the prefix over earlier CTAs, from each expert's contiguous count row
+    const int b = blockIdx.x;
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+      const uint4* row = reinterpret_cast<const uint4*>(a.counts + (int64_t)e * a.row);
+      uint32_t tot = 0, pre = 0;
+#pragma unroll 16
+      for (int q = 0; q < a.row / 4; ++q) {
+        const uint4 c = row[q];
+        tot += c.x + c.y + c.z + c.w;
+        pre += (4 * q < b ? c.x : 0u) + (4 * q + 1 < b ? c.y : 0u) + (4 * q + 2 < b ? c.z : 0u) +
+               (4 * q + 3 < b ? c.w : 0u);
+      }
+      s_base[e] = tot;
+      s_pre[e] = pre;
+    }
+    if (threadIdx.x == 0) s_flags = 0;
+    __syncthreads();
+    emit_expert_table(a, s_base, s_act, warp_tmp, b == 0);  // s_base[e] := start(e)
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
+    if (b == 0) {
+      uint32_t f = 0;
+      for (int j = threadIdx.x; j < a.num_blocks; j += kIdxThreads) f |= a.flags[j];
+      f = __reduce_or_sync(kFullMask, f);
+      if (lane == 0 && f) atomicOr(&s_flags, f);
+      __syncthreads();
+      if (threadIdx.x == 0) *a.status = s_flags;
+    }
   } else {
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
-      s_base[e] = a.counts[(int64_t)blockIdx.x * a.E + e];
+      s_base[e] = a.counts[(int64_t)e * a.row + blockIdx.x];
   }
   __syncthreads();
   // per-warp running offsets: base + slots of e in earlier warps
@@ -311,6 +366,24 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
       if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
     }
   }
+}
+
+moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream) {
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 3) * a.E;
+  if (L.num_blocks <= 1) {
+    return launch(idx_scatter_kernel<kBasesSingleCta>, 1, kIdxThreads, scatter_smem, stream, a);
+  }
+  moe_status_t st =
+      launch(idx_count_kernel, a.num_blocks, kIdxThreads, sizeof(uint32_t) * a.E, stream, a);
+  if (st != MOE_OK) return st;
+  if (L.row * a.E <= kMaxSharedCountWords)
+    return launch(idx_scatter_kernel<kBasesFromCounts>, a.num_blocks, kIdxThreads, scatter_smem,
+                  stream, a);
+  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
+  st = launch(idx_scan_kernel, 1, kScanThreads, scan_smem, stream, a);
+  if (st != MOE_OK) return st;
+  return launch(idx_scatter_kernel<kBasesFromScan>, a.num_blocks, kIdxThreads, scatter_smem,
+                stream, a);
 }
 
 }  // namespace
@@ -359,17 +432,8 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   a.N = (uint32_t)N;
   a.E = E;
   a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);
-
-  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 2) * E;
-  if (L.num_blocks <= 1) {
-    idx_scatter_kernel<true><<<1, kIdxThreads, scatter_smem, stream>>>(a);
-    return launch_status();
-  }
-  idx_count_kernel<<<a.num_blocks, kIdxThreads, sizeof(uint32_t) * E, stream>>>(a);
-  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
-  idx_scan_kernel<<<1, kScanThreads, scan_smem, stream>>>(a);
-  idx_scatter_kernel<false><<<a.num_blocks, kIdxThreads, scatter_smem, stream>>>(a);
-  return launch_status();
+  a.row = (int)L.row;
+  return launch_index(a, L, stream);
 }
 
 extern "C" moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,
@@ -457,15 +521,6 @@ extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order
   a.N = (uint32_t)N;
   a.E = E;
   a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);
-
-  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 2) * E;
-  if (L.num_blocks <= 1) {
-    idx_scatter_kernel<true><<<1, kIdxThreads, scatter_smem, stream>>>(a);
-    return launch_status();
-  }
-  idx_count_kernel<<<a.num_blocks, kIdxThreads, sizeof(uint32_t) * E, stream>>>(a);
-  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
-  idx_scan_kernel<<<1, kScanThreads, scan_smem, stream>>>(a);
-  idx_scatter_kernel<false><<<a.num_blocks, kIdxThreads, scatter_smem, stream>>>(a);
-  return launch_status();
+  a.row = (int)L.row;
+  return launch_index(a, L, stream);
 }

@@ -63,6 +63,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // K known at compile time: all K row loads of kChunkUnroll chunks in flight.
 template <int K>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) {
+  wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
     int64_t row[K];
     float w[K];
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) 
 
 // Any K <= 32: one row load per step, chunks unrolled for some overlap.
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinArgs a) {
+  wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
     uint4* out_row = a.out + t * a.H8;
     for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kFinThreads * kChunkUnroll) {
@@ -138,8 +140,7 @@ moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream) {
     per_sm = 1;
   const int64_t cap = (int64_t)device_info().sm_count * per_sm;
   const int grid = (int)(a.T < cap ? a.T : cap);
-  k<<<grid, kFinThreads, 0, stream>>>(a);
-  return launch_status();
+  return launch(k, grid, kFinThreads, 0, stream, a);
 }
 
 }  // namespace

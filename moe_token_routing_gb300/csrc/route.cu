@@ -58,6 +58,7 @@ __device__ __forceinline__ void top2_push(float& t1, float& t2, float x) {
 // Lane j < G holds g_j on entry.
 __device__ __forceinline__ uint32_t keep_best_groups(float gj, int lane, int G, int M) {
   int ahead = 0;
+#pragma unroll 8
   for (int j = 0; j < G; ++j) {
     const float gx = __shfl_sync(kFullMask, gj, j);
     ahead += (gx > gj) || (gx == gj && j < lane);
@@ -65,65 +66,99 @@ __device__ __forceinline__ uint32_t keep_best_groups(float gj, int lane, int G, 
   return __ballot_sync(kFullMask, lane < G && ahead < M);
 }
 
+// The C scores of row t that lane l owns (experts l*C .. l*C+C-1).
 template <int C, bool kVec>
-__global__ void __launch_bounds__(kRouteThreads) route_warp_kernel(const RouteArgs a) {
+__device__ __forceinline__ void load_lane_scores(const RouteArgs& a, int64_t t, int e0,
+                                                 const bool (&valid)[C], float (&s)[C]) {
+  const float* row = a.scores + t * a.E;
+  if constexpr (kVec) {
+#pragma unroll
+    for (int q = 0; q < C / 4; ++q) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + 4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + e0 + 4 * q));
+      s[4 * q + 0] = v.x;
+      s[4 * q + 1] = v.y;
+      s[4 * q + 2] = v.z;
+      s[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < C; ++c) s[c] = valid[c] ? __ldg(row + e0 + c) : 0.0f;
+  }
+}
+
+// Exact top-K by K rounds of a warp-wide max over each lane's best key; the
+// winning lane recomputes its best from all of its keys. Returns, in lane r <
+// K, the expert chosen in round r.
+template <int C>
+__device__ __forceinline__ int select_by_full_rounds(uint32_t (&key)[C], int lane, int e0, int K) {
+  uint32_t head = 0;
+  int head_pos = 0;
+#pragma unroll
+  for (int c = 0; c < C; ++c)
+    if (key[c] > head) { head = key[c]; head_pos = c; }
+  int my_id = 0;
+  for (int r = 0; r < K; ++r) {
+    const uint32_t best = __reduce_max_sync(kFullMask, head);
+    const unsigned holders = __ballot_sync(kFullMask, head == best && head != 0u);
+    const int win_lane = holders ? __ffs(holders) - 1 : 0;
+    const int id = __shfl_sync(kFullMask, e0 + head_pos, win_lane);
+    if (lane == r) my_id = id;
+    if (lane == win_lane) {
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        if (c == head_pos) key[c] = 0u;
+      head = 0;
+      head_pos = 0;
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        if (key[c] > head) { head = key[c]; head_pos = c; }
+    }
+  }
+  return my_id;
+}
+
+template <int C, bool kVec>
+__global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kernel(const RouteArgs a) {
+  static_assert(C >= 2, "the warp path holds at least two experts per lane");
   extern __shared__ float dyn_smem[];  // kGroupsGeneric: kRouteWarps * E biased scores
+  wait_for_prior_grid();
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int e0 = lane * C;
 
   float bias_r[C];
-  int grp[C];
   bool valid[C];
+  int n_valid = 0;
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     const int e = e0 + c;
     valid[c] = e < a.E;
     bias_r[c] = valid[c] ? a.bias[e] : 0.0f;
-    grp[c] = valid[c] ? e / a.S : 31;
+    n_valid += valid[c];
   }
+  // In the segment layout a lane's experts all belong to one group.
+  const int lane_grp = n_valid > 0 ? e0 / a.S : 31;
 
   const int64_t first = (int64_t)blockIdx.x * kRouteWarps + warp;
   const int64_t stride = (int64_t)gridDim.x * kRouteWarps;
+  float s_next[C];
+  if (first < a.T) load_lane_scores<C, kVec>(a, first, e0, valid, s_next);
+
   for (int64_t t = first; t < a.T; t += stride) {
-    const float* row = a.scores + t * a.E;
     float s[C];
-    if constexpr (kVec) {
 #pragma unroll
-      for (int q = 0; q < C / 4; ++q) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (e0 + 4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + e0 + 4 * q));
-        s[4 * q + 0] = v.x;
-        s[4 * q + 1] = v.y;
-        s[4 * q + 2] = v.z;
-        s[4 * q + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < C; ++c) s[c] = valid[c] ? __ldg(row + e0 + c) : 0.0f;
-    }
+    for (int c = 0; c < C; ++c) s[c] = s_next[c];
+    if (t + stride < a.T) load_lane_scores<C, kVec>(a, t + stride, e0, valid, s_next);
+
     float b[C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) b[c] = __fadd_rn(s[c], bias_r[c]);
+    for (int c = 0; c < C; ++c) b[c] = valid[c] ? __fadd_rn(s[c], bias_r[c]) : -CUDART_INF_F;
 
-    // ---- group selection ----
-    uint32_t kept = kFullMask;
-    if (a.group_mode == kGroupsSegment) {
-      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        if (valid[c]) top2_push(t1, t2, b[c]);
-      for (int off = 1; off < a.seg_lanes; off <<= 1) {
-        const float o1 = __shfl_xor_sync(kFullMask, t1, off);
-        const float o2 = __shfl_xor_sync(kFullMask, t2, off);
-        t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
-        t1 = fmaxf(t1, o1);
-      }
-      const float g = __fadd_rn(t1, t2);
-      const float gj = __shfl_sync(kFullMask, g, lane < a.G ? lane * a.seg_lanes : 0);
-      kept = keep_best_groups(gj, lane, a.G, a.M);
-    } else if (a.group_mode == kGroupsGeneric) {
+    int my_id = 0;
+    if (a.group_mode == kGroupsGeneric) {
+      // ---- groups through shared memory, then the exact full-round selection ----
       float* wb = dyn_smem + warp * a.E;
 #pragma unroll
       for (int c = 0; c < C; ++c)
@@ -136,43 +171,97 @@ __global__ void __launch_bounds__(kRouteThreads) route_warp_kernel(const RouteAr
         gj = (a.S == 1) ? t1 : __fadd_rn(t1, t2);
       }
       __syncwarp();
-      kept = keep_best_groups(gj, lane, a.G, a.M);
-    }
-
-    // ---- expert top-K over the kept groups ----
-    uint32_t key[C];
+      const uint32_t kept = keep_best_groups(gj, lane, a.G, a.M);
+      uint32_t key[C];
 #pragma unroll
-    for (int c = 0; c < C; ++c)
-      key[c] = (valid[c] && ((kept >> grp[c]) & 1u)) ? ordered_key(b[c]) : 0u;
-    uint32_t head = 0;
-    int head_pos = 0;
+      for (int c = 0; c < C; ++c)
+        key[c] = (valid[c] && ((kept >> ((e0 + c) / a.S)) & 1u)) ? ordered_key(b[c]) : 0u;
+      my_id = select_by_full_rounds<C>(key, lane, e0, a.K);
+    } else {
+      // ---- lane cache: the two best biased scores and their positions ----
+      // (ties keep the lower position, so cached entries come in expert order)
+      float v1, v2;
+      int p1, p2;
+      if (b[1] > b[0]) { v1 = b[1]; p1 = 1; v2 = b[0]; p2 = 0; }
+      else { v1 = b[0]; p1 = 0; v2 = b[1]; p2 = 1; }
 #pragma unroll
-    for (int c = 0; c < C; ++c)
-      if (key[c] > head) { head = key[c]; head_pos = c; }
+      for (int c = 2; c < C; ++c) {
+        const float x = b[c];
+        const bool g1 = x > v1, g2 = x > v2;
+        v2 = g1 ? v1 : (g2 ? x : v2);
+        p2 = g1 ? p1 : (g2 ? c : p2);
+        v1 = g1 ? x : v1;
+        p1 = g1 ? c : p1;
+      }
 
-    int my_id = 0;
-    for (int r = 0; r < a.K; ++r) {
-      const uint32_t best = __reduce_max_sync(kFullMask, head);
-      const unsigned holders = __ballot_sync(kFullMask, head == best && head != 0u);
-      const int win_lane = holders ? __ffs(holders) - 1 : 0;
-      const int id = __shfl_sync(kFullMask, e0 + head_pos, win_lane);
-      if (lane == r) my_id = id;
-      if (lane == win_lane) {
+      // ---- group selection (segment layout: the group's top-2 over its lanes) ----
+      bool lane_allowed = n_valid > 0;
+      if (a.group_mode == kGroupsSegment) {
+        float t1 = n_valid > 0 ? v1 : -CUDART_INF_F, t2 = n_valid > 0 ? v2 : -CUDART_INF_F;
+        for (int off = 1; off < a.seg_lanes; off <<= 1) {
+          const float o1 = __shfl_xor_sync(kFullMask, t1, off);
+          const float o2 = __shfl_xor_sync(kFullMask, t2, off);
+          t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+          t1 = fmaxf(t1, o1);
+        }
+        const float g = __fadd_rn(t1, t2);
+        const float gj = __shfl_sync(kFullMask, g, lane < a.G ? lane * a.seg_lanes : 0);
+        const uint32_t kept = keep_best_groups(gj, lane, a.G, a.M);
+        lane_allowed = lane_allowed && ((kept >> lane_grp) & 1u);
+      }
+      const int n_allowed = lane_allowed ? n_valid : 0;
+
+      // ---- K rounds of a warp-wide max over the cached heads ----
+      uint32_t k1 = (n_allowed >= 1) ? ordered_key(v1) : 0u;
+      uint32_t k2 = (n_allowed >= 2) ? ordered_key(v2) : 0u;
+      int i1 = e0 + p1, i2 = e0 + p2;
+      const int q1 = p1, q2 = p2;
+      int wins = 0;
+      uint32_t kth = 0;
+      int kth_id = 0;
+#pragma unroll 8
+      for (int r = 0; r < a.K; ++r) {
+        const uint32_t best = __reduce_max_sync(kFullMask, k1);
+        const unsigned holders = __ballot_sync(kFullMask, k1 == best);
+        const int win_lane = __ffs(holders) - 1;
+        const int id = __shfl_sync(kFullMask, i1, win_lane);
+        if (lane == r) my_id = id;
+        kth = best;
+        kth_id = id;
+        if (lane == win_lane) {
+          k1 = k2;
+          i1 = i2;
+          k2 = 0u;
+          ++wins;
+        }
+      }
+
+      // ---- exactness check: a lane that gave up both cached entries may hold
+      // a third candidate that should have won a later round ----
+      const bool needs3 = wins == 2 && n_allowed > 2;
+      if (__any_sync(kFullMask, needs3) || kth == 0u) {
+        float v3 = -CUDART_INF_F;
+        int c3 = -1;
 #pragma unroll
         for (int c = 0; c < C; ++c)
-          if (c == head_pos) key[c] = 0u;
-        head = 0;
-        head_pos = 0;
+          if (valid[c] && c != q1 && c != q2 && (c3 < 0 || b[c] > v3)) { v3 = b[c]; c3 = c; }
+        const uint32_t k3 = ordered_key(v3);
+        const bool beats = k3 > kth || (k3 == kth && e0 + c3 < kth_id);
+        if (kth == 0u || __any_sync(kFullMask, needs3 && beats)) {
+          uint32_t key[C];
 #pragma unroll
-        for (int c = 0; c < C; ++c)
-          if (key[c] > head) { head = key[c]; head_pos = c; }
+          for (int c = 0; c < C; ++c) key[c] = (valid[c] && lane_allowed) ? ordered_key(b[c]) : 0u;
+          my_id = select_by_full_rounds<C>(key, lane, e0, a.K);
+        }
       }
     }
 
     // ---- weights: unbiased score, optional normalisation, scaling ----
+    const float* row = a.scores + t * a.E;
     float w = (lane < a.K) ? __ldg(row + my_id) : 0.0f;
     if (a.norm) {
       float sum = 0.0f;
+#pragma unroll 8
       for (int k = 0; k < a.K; ++k) sum = __fadd_rn(sum, __shfl_sync(kFullMask, w, k));
       w = __fdiv_rn(w, sum);
     }
@@ -187,6 +276,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_warp_kernel(const RouteAr
 // One thread per token, E <= EP <= 32.
 template <int EP, bool kVec>
 __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const RouteArgs a) {
+  wait_for_prior_grid();
   float bias_r[EP];
   uint32_t valid = 0, run_start = 0, run_end = 0;
 #pragma unroll
@@ -306,8 +396,7 @@ moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, 
   const int64_t want = (a.T + tokens_per_cta - 1) / tokens_per_cta;
   const int64_t cap = (int64_t)device_info().sm_count * ctas_per_sm(k, smem);
   const int grid = (int)(want < cap ? want : cap);
-  k<<<grid, kRouteThreads, smem, stream>>>(a);
-  return launch_status();
+  return launch(k, grid, kRouteThreads, smem, stream, a);
 }
 
 template <int C>
