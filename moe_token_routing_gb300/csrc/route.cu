@@ -178,26 +178,36 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
         key[c] = (valid[c] && ((kept >> ((e0 + c) / a.S)) & 1u)) ? ordered_key(b[c]) : 0u;
       my_id = select_by_full_rounds<C>(key, lane, e0, a.K);
     } else {
-      // ---- lane cache: the two best biased scores and their positions ----
-      // (ties keep the lower position, so cached entries come in expert order)
-      float v1, v2;
-      int p1, p2;
-      if (b[1] > b[0]) { v1 = b[1]; p1 = 1; v2 = b[0]; p2 = 0; }
-      else { v1 = b[0]; p1 = 0; v2 = b[1]; p2 = 1; }
+      // ---- lane cache: the D best biased scores and their positions ----
+      // (ties keep the lower position, so equal entries come in expert order)
+      constexpr int D = C >= 3 ? 3 : 2;
+      float v[D];
+      int p[D];
 #pragma unroll
-      for (int c = 2; c < C; ++c) {
+      for (int j = 0; j < D; ++j) {
+        v[j] = 0.0f;
+        p[j] = 0;
+      }
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
         const float x = b[c];
-        const bool g1 = x > v1, g2 = x > v2;
-        v2 = g1 ? v1 : (g2 ? x : v2);
-        p2 = g1 ? p1 : (g2 ? c : p2);
-        v1 = g1 ? x : v1;
-        p1 = g1 ? c : p1;
+        bool g[D];
+#pragma unroll
+        for (int j = 0; j < D; ++j) g[j] = (j >= c) || x > v[j];  // empty slots take x
+#pragma unroll
+        for (int j = D - 1; j >= 1; --j) {
+          if (j > c) continue;
+          v[j] = g[j - 1] ? v[j - 1] : (g[j] ? x : v[j]);
+          p[j] = g[j - 1] ? p[j - 1] : (g[j] ? c : p[j]);
+        }
+        v[0] = g[0] ? x : v[0];
+        p[0] = g[0] ? c : p[0];
       }
 
       // ---- group selection (segment layout: the group's top-2 over its lanes) ----
       bool lane_allowed = n_valid > 0;
       if (a.group_mode == kGroupsSegment) {
-        float t1 = n_valid > 0 ? v1 : -CUDART_INF_F, t2 = n_valid > 0 ? v2 : -CUDART_INF_F;
+        float t1 = n_valid > 0 ? v[0] : -CUDART_INF_F, t2 = n_valid > 0 ? v[1] : -CUDART_INF_F;
         for (int off = 1; off < a.seg_lanes; off <<= 1) {
           const float o1 = __shfl_xor_sync(kFullMask, t1, off);
           const float o2 = __shfl_xor_sync(kFullMask, t2, off);
@@ -212,42 +222,52 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
       const int n_allowed = lane_allowed ? n_valid : 0;
 
       // ---- K rounds of a warp-wide max over the cached heads ----
-      uint32_t k1 = (n_allowed >= 1) ? ordered_key(v1) : 0u;
-      uint32_t k2 = (n_allowed >= 2) ? ordered_key(v2) : 0u;
-      int i1 = e0 + p1, i2 = e0 + p2;
-      const int q1 = p1, q2 = p2;
+      uint32_t k[D];
+      int id[D];
+#pragma unroll
+      for (int j = 0; j < D; ++j) {
+        k[j] = n_allowed > j ? ordered_key(v[j]) : 0u;
+        id[j] = e0 + p[j];
+      }
       int wins = 0;
       uint32_t kth = 0;
       int kth_id = 0;
 #pragma unroll 8
       for (int r = 0; r < a.K; ++r) {
-        const uint32_t best = __reduce_max_sync(kFullMask, k1);
-        const unsigned holders = __ballot_sync(kFullMask, k1 == best);
+        const uint32_t best = __reduce_max_sync(kFullMask, k[0]);
+        const unsigned holders = __ballot_sync(kFullMask, k[0] == best);
         const int win_lane = __ffs(holders) - 1;
-        const int id = __shfl_sync(kFullMask, i1, win_lane);
-        if (lane == r) my_id = id;
+        const int win_id = __shfl_sync(kFullMask, id[0], win_lane);
+        if (lane == r) my_id = win_id;
         kth = best;
-        kth_id = id;
+        kth_id = win_id;
         if (lane == win_lane) {
-          k1 = k2;
-          i1 = i2;
-          k2 = 0u;
+#pragma unroll
+          for (int j = 0; j + 1 < D; ++j) {
+            k[j] = k[j + 1];
+            id[j] = id[j + 1];
+          }
+          k[D - 1] = 0u;
           ++wins;
         }
       }
 
-      // ---- exactness check: a lane that gave up both cached entries may hold
-      // a third candidate that should have won a later round ----
-      const bool needs3 = wins == 2 && n_allowed > 2;
-      if (__any_sync(kFullMask, needs3) || kth == 0u) {
-        float v3 = -CUDART_INF_F;
-        int c3 = -1;
+      // ---- exactness check: a lane that gave up all D cached entries may hold
+      // a further candidate that should have won a later round ----
+      const bool needs_more = wins == D && n_allowed > D;
+      if (__any_sync(kFullMask, needs_more) || kth == 0u) {
+        float vn = -CUDART_INF_F;
+        int cn = -1;
 #pragma unroll
-        for (int c = 0; c < C; ++c)
-          if (valid[c] && c != q1 && c != q2 && (c3 < 0 || b[c] > v3)) { v3 = b[c]; c3 = c; }
-        const uint32_t k3 = ordered_key(v3);
-        const bool beats = k3 > kth || (k3 == kth && e0 + c3 < kth_id);
-        if (kth == 0u || __any_sync(kFullMask, needs3 && beats)) {
+        for (int c = 0; c < C; ++c) {
+          bool cached = false;
+#pragma unroll
+          for (int j = 0; j < D; ++j) cached = cached || c == p[j];
+          if (valid[c] && !cached && (cn < 0 || b[c] > vn)) { vn = b[c]; cn = c; }
+        }
+        const uint32_t kn = ordered_key(vn);
+        const bool beats = kn > kth || (kn == kth && e0 + cn < kth_id);
+        if (kth == 0u || __any_sync(kFullMask, needs_more && beats)) {
           uint32_t key[C];
 #pragma unroll
           for (int c = 0; c < C; ++c) key[c] = (valid[c] && lane_allowed) ? ordered_key(b[c]) : 0u;
