@@ -8,10 +8,10 @@ from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, EXPORTED_SYMBOLS, IndexBuffer
                       MoeLibraryMissing, create_indices, finalize, load_library,
                       moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
                       moe_read_device_status, moe_route, route)
-from .pipeline import RoutingPipeline
+from .pipeline import HostStreamer, RoutingPipeline
 
 __all__ = [
-    "DEVICE_STATUS_BAD_EXPERT_ID", "EXPORTED_SYMBOLS", "IndexBuffers", "MoeError",
+    "DEVICE_STATUS_BAD_EXPERT_ID", "EXPORTED_SYMBOLS", "HostStreamer", "IndexBuffers", "MoeError",
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
     "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
     "moe_read_device_status", "moe_route", "route",

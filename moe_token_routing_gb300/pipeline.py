@@ -37,9 +37,9 @@ class RoutingPipeline:
     def create_indices(self, stream=None):
         self.index.run(self.expert_indices, stream)
 
-    def finalize(self, down, stream=None):
-        moe_finalize(self.output, down, self.index.restore_token_order, self.expert_weights,
-                     stream)
+    def finalize(self, down, stream=None, output=None):
+        moe_finalize(self.output if output is None else output, down,
+                     self.index.restore_token_order, self.expert_weights, stream)
 
     def __call__(self, expert_scores, expert_bias, down, stream=None) -> torch.Tensor:
         self.route(expert_scores, expert_bias, stream)
@@ -71,7 +71,72 @@ class RoutingPipeline:
             out_h.copy_(self.output, non_blocking=True)
         return out_h
 
+    def stream_from_host(self, depth: int = 2) -> "HostStreamer":
+        """A double-buffered host-buffer runner over this pipeline (see HostStreamer)."""
+        return HostStreamer(self, depth)
+
     def host_bytes(self) -> tuple[int, int]:
         """(host-to-device, device-to-host) bytes that run_host moves per call."""
         h2d = self.T * self.E * 4 + self.E * 4 + self.T * self.K * self.H * 2
         return h2d, self.T * self.H * 2
+
+
+class HostStreamer:
+    """Runs a sequence of batches from host (pinned) buffers through a
+    RoutingPipeline with the copies overlapped: while batch i computes and
+    its output is copied back, batch i+1's inputs are already being copied in.
+
+    Three CUDA streams (copy-in, compute, copy-out) and ``depth`` sets of
+    device staging and output buffers; events order each batch's copy-in ->
+    compute -> copy-out and keep a staging set from being overwritten before
+    the compute that reads it is done. ``submit`` only enqueues; call
+    ``synchronize`` before reading the host outputs.
+    """
+
+    def __init__(self, pipe: RoutingPipeline, depth: int = 2):
+        self.pipe = pipe
+        self.depth = depth
+        d = pipe.device
+        self.copy_in = torch.cuda.Stream(d)
+        self.compute = torch.cuda.Stream(d)
+        self.copy_out = torch.cuda.Stream(d)
+        T, E, K, H = pipe.T, pipe.E, pipe.K, pipe.H
+        self.slots = []
+        for _ in range(depth):
+            self.slots.append({
+                "scores": torch.empty((T, E), dtype=torch.float32, device=d),
+                "bias": torch.empty((E,), dtype=torch.float32, device=d),
+                "down": torch.empty((T * K, H), dtype=torch.bfloat16, device=d),
+                "out": torch.empty((T, H), dtype=torch.bfloat16, device=d),
+                "copied_in": torch.cuda.Event(), "computed": torch.cuda.Event(),
+                "copied_out": torch.cuda.Event(), "used": False,
+            })
+        self.count = 0
+
+    def submit(self, scores_h: torch.Tensor, bias_h: torch.Tensor, down_h: torch.Tensor,
+               out_h: torch.Tensor) -> None:
+        slot = self.slots[self.count % self.depth]
+        if slot["used"]:
+            self.copy_in.wait_event(slot["computed"])     # staging no longer read
+            self.compute.wait_event(slot["copied_out"])   # output no longer read
+        with torch.cuda.stream(self.copy_in):
+            slot["scores"].copy_(scores_h, non_blocking=True)
+            slot["bias"].copy_(bias_h, non_blocking=True)
+            slot["down"].copy_(down_h, non_blocking=True)
+            slot["copied_in"].record(self.copy_in)
+        self.compute.wait_event(slot["copied_in"])
+        self.pipe.route(slot["scores"], slot["bias"], self.compute)
+        self.pipe.create_indices(self.compute)
+        self.pipe.finalize(slot["down"], self.compute, output=slot["out"])
+        slot["computed"].record(self.compute)
+        self.copy_out.wait_event(slot["computed"])
+        with torch.cuda.stream(self.copy_out):
+            out_h.copy_(slot["out"], non_blocking=True)
+            slot["copied_out"].record(self.copy_out)
+        slot["used"] = True
+        self.count += 1
+
+    def synchronize(self) -> None:
+        self.copy_out.synchronize()
+        self.compute.synchronize()
+        self.copy_in.synchronize()

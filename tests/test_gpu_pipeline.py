@@ -53,3 +53,32 @@ def test_host_buffer_call(name):
         ref = workload_finalize_ref(name)
         got = out_h.view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(got, f32_to_bf16_bits(ref))
+
+
+def test_host_streamer_overlapped_batches():
+    """HostStreamer: several batches with different inputs, copies overlapped
+    across batches; every output equals the synchronous host-buffer call's."""
+    import synth
+    cfg0 = synth.get_config("dsv3_decode")
+    pipe = _pipe(cfg0)
+    batches = []
+    for seed in (3, 4, 5, 6, 7):
+        c = cfg0.replace(seed=seed)
+        s_h = torch.from_numpy(synth.make_scores(c)).pin_memory()
+        b_h = torch.from_numpy(synth.make_bias(c)).pin_memory()
+        d_h = torch.from_numpy(synth.make_down(c).view(np.int16)).view(torch.bfloat16).pin_memory()
+        batches.append((s_h, b_h, d_h))
+    expected = []
+    for s_h, b_h, d_h in batches:
+        out_h = torch.empty((c.T, c.H), dtype=torch.bfloat16).pin_memory()
+        pipe.run_host(s_h, b_h, d_h, out_h)
+        torch.cuda.synchronize()
+        expected.append(out_h.clone())
+    streamer = pipe.stream_from_host(depth=2)
+    outs = [torch.zeros((c.T, c.H), dtype=torch.bfloat16).pin_memory() for _ in batches]
+    for (s_h, b_h, d_h), out_h in zip(batches, outs):
+        streamer.submit(s_h, b_h, d_h, out_h)
+    streamer.synchronize()
+    for got, exp in zip(outs, expected):
+        assert torch.equal(got.view(torch.int16), exp.view(torch.int16))
+    assert not torch.equal(expected[0].view(torch.int16), expected[1].view(torch.int16))
