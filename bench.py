@@ -347,6 +347,24 @@ def run_gpu(args, cfg, rank, world, local_rank):
     # correctness spot check of this run's output against the first token rows
     out_ok = bool(torch.isfinite(pipe.output[:4].float()).all().item())
 
+    # ---- next row (not in the step): expert-contiguous token rows for the grouped matmul
+    x_h = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, pin_memory=True)
+    import synth
+    synth.make_input(cfg.replace(seed=cfg.seed + rank), out_ptr=x_h.data_ptr())
+    x_d = x_h.to(dev)
+    perm_out = torch.empty((cfg.N, cfg.H), dtype=torch.bfloat16, device=dev)
+    pipe.permute(x_d, perm_out)
+    kp = min(K, 100)
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kp)]
+    for i in range(kp):
+        flush.zero_()
+        pev[i][0].record(stream)
+        pipe.permute(x_d, perm_out)
+        pev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    perm_ms = statistics.fmean([e[0].elapsed_time(e[1]) for e in pev])
+    del perm_out, x_d
+
     # ---- end to end through the host-buffer API: pinned inputs copied in and the
     # output copied back every step, copies of consecutive steps overlapped
     s_h = torch.from_numpy(scores).pin_memory()
@@ -413,6 +431,13 @@ def run_gpu(args, cfg, rank, world, local_rank):
                       "note": "route/create_indices/finalize from a separate pass with an event "
                               "between every stage; the timed steps carry events only at the "
                               "step start, before finalize and at the step end"},
+        "next_rows": {"permute": {
+            "ms": perm_ms, "tokens_per_s": cfg.T / (perm_ms * 1e-3),
+            "achieved_gbs": (2 * cfg.T * cfg.H + 2 * cfg.N * cfg.H + 4 * cfg.N) / (perm_ms * 1e-3) / 1e9,
+            "frac_of_peak": (2 * cfg.T * cfg.H + 2 * cfg.N * cfg.H + 4 * cfg.N)
+            / (perm_ms * 1e-3) / 1e9 / peak,
+            "algorithmic_bytes": 2 * cfg.T * cfg.H + 2 * cfg.N * cfg.H + 4 * cfg.N,
+            "note": "measured after the timed steps; not part of the step"}},
         "stages_tokens_per_s": {"route": cfg.T / (route_mean * 1e-3),
                                 "create_indices": cfg.T / (statistics.fmean(index_ms) * 1e-3),
                                 "finalize": cfg.T / (fin_mean * 1e-3)},

@@ -41,6 +41,9 @@ extern "C" {
 /* Raw bf16 bit pattern (1 sign, 8 exponent, 7 mantissa bits), as in __nv_bfloat16. */
 typedef uint16_t moe_bf16_t;
 
+/* Element types of the dtype-generic entry points. */
+typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype_t;
+
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
@@ -157,6 +160,44 @@ moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
                           const uint32_t* restore_order, const float* router_weight,
                           int64_t num_tokens, int32_t num_experts_per_token, int64_t hidden,
                           cudaStream_t stream);
+
+/*
+ * moe_finalize_ex -- moe_finalize with the router-weight and output element
+ * types as arguments.
+ * Page "moe_finalize": Parameters weight_type and out_type (the page's
+ * kernel is generic over them; down_type stays bf16 here).
+ *
+ * Same sum as moe_finalize, accumulated in fp32 (a bf16 weight widens to fp32
+ * exactly). output_dtype MOE_DTYPE_BF16 rounds each sum to nearest-even bf16;
+ * MOE_DTYPE_F32 stores the fp32 sum itself.
+ * output [T, H] of output_dtype, 16-byte aligned. router_weight [T, K] of
+ * weight_dtype, aligned to its element size. Other arguments and rules as in
+ * moe_finalize; an unknown dtype returns MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype, const moe_bf16_t* down,
+                             const uint32_t* restore_order, const void* router_weight,
+                             moe_dtype_t weight_dtype, int64_t num_tokens,
+                             int32_t num_experts_per_token, int64_t hidden, cudaStream_t stream);
+
+/*
+ * moe_permute -- expert-contiguous copy of the token rows, the input of the
+ * grouped matmul that sits between moe_create_indices and moe_finalize.
+ * Page "moe_create_indices": description paragraph (tokens are grouped by
+ * expert so that downstream kernels such as grouped matmul can process each
+ * expert's tokens contiguously).
+ *
+ *   permuted[restore_token_order[t*K+k], :] = input[t, :]   for t < T, k < K
+ * so row p of permuted is input[token_expert_order[p] / K].
+ *
+ * permuted [T*K, H] bf16 out. input [T, H] bf16 in. restore_token_order
+ * [T*K] uint32 in (as written by moe_create_indices).
+ * Requirements: T >= 0; 1 <= K <= MOE_MAX_EXPERTS_PER_TOK; T*K < 2^32; H >= 0
+ * and H % 8 == 0; permuted and input 16-byte aligned and not overlapping;
+ * restore_token_order 4-byte aligned. An entry >= T*K is skipped.
+ */
+moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* input,
+                         const uint32_t* restore_token_order, int64_t num_tokens,
+                         int32_t num_experts_per_token, int64_t hidden, cudaStream_t stream);
 
 /*
  * Reads the device status word that the last moe_create_indices call on

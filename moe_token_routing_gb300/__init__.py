@@ -7,12 +7,12 @@ kernel behind the C ABI of libmoe_routing.so (include/moe_routing.h).
 from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, EXPORTED_SYMBOLS, IndexBuffers, MoeError,
                       MoeLibraryMissing, create_indices, finalize, load_library,
                       moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
-                      moe_read_device_status, moe_route, route)
+                      moe_finalize_ex, moe_permute, moe_read_device_status, moe_route, permute, route)
 from .pipeline import HostStreamer, RoutingPipeline
 
 __all__ = [
     "DEVICE_STATUS_BAD_EXPERT_ID", "EXPORTED_SYMBOLS", "HostStreamer", "IndexBuffers", "MoeError",
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
     "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
-    "moe_read_device_status", "moe_route", "route",
+    "moe_finalize_ex", "moe_permute", "moe_read_device_status", "moe_route", "permute", "route",
 ]

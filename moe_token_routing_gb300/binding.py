@@ -26,7 +26,7 @@ DEVICE_STATUS_BAD_EXPERT_ID = 0x1
 # Entry points declared in include/moe_routing.h.
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
                     "moe_create_indices", "moe_finalize", "moe_read_device_status",
-                    "moe_create_indices_no_alloc")
+                    "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex")
 
 
 class MoeError(RuntimeError):
@@ -65,6 +65,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_finalize.restype = ctypes.c_int
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_read_device_status.restype = ctypes.c_int
+    lib.moe_permute.argtypes = [vp, vp, vp, i64, i32, i64, vp]
+    lib.moe_permute.restype = ctypes.c_int
+    lib.moe_finalize_ex.argtypes = [vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, i64, i32, i64, vp]
+    lib.moe_finalize_ex.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -152,6 +156,39 @@ def moe_finalize(output: torch.Tensor, down: torch.Tensor, restore_order: torch.
     _check("moe_finalize", rc)
 
 
+def moe_permute(permuted: torch.Tensor, input: torch.Tensor, restore_token_order: torch.Tensor,
+                stream=None) -> None:
+    """permuted[restore_token_order[t*K+k]] = input[t]: the expert-contiguous token rows."""
+    T, H = input.shape
+    N = restore_token_order.numel()
+    K = N // T if T else 1
+    if T and N != T * K:
+        raise ValueError("restore_token_order must have T*K entries")
+    args = (_dev(permuted, "permuted", torch.bfloat16, (N, H)),
+            _dev(input, "input", torch.bfloat16),
+            _dev(restore_token_order, "restore_token_order", torch.int32, (N,)))
+    _check("moe_permute", load_library().moe_permute(*args, T, K, H, _stream(stream)))
+
+
+_DTYPE_CODES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+def moe_finalize_ex(output: torch.Tensor, down: torch.Tensor, restore_order: torch.Tensor,
+                    router_weight: torch.Tensor, stream=None) -> None:
+    """moe_finalize with bf16 or fp32 router weights and a bf16 or fp32 output
+    (taken from the tensors' dtypes)."""
+    T, K = router_weight.shape
+    H = down.shape[1]
+    if output.dtype not in _DTYPE_CODES or router_weight.dtype not in _DTYPE_CODES:
+        raise TypeError("output and router_weight must be bfloat16 or float32")
+    args = (_dev(output, "output", output.dtype, (T, H)), _DTYPE_CODES[output.dtype],
+            _dev(down, "down", torch.bfloat16, (T * K, H)),
+            _dev(restore_order, "restore_order", torch.int32, (T * K,)),
+            _dev(router_weight, "router_weight", router_weight.dtype, (T, K)),
+            _DTYPE_CODES[router_weight.dtype])
+    _check("moe_finalize_ex", load_library().moe_finalize_ex(*args, T, K, H, _stream(stream)))
+
+
 def moe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     """Device status word of the last moe_create_indices on this workspace (synchronises)."""
     out = ctypes.c_uint32(0)
@@ -229,6 +266,13 @@ class IndexBuffers:
 
 def create_indices(topk_ids: torch.Tensor, n_experts: int, stream=None) -> IndexBuffers:
     return IndexBuffers(topk_ids.numel(), n_experts, topk_ids.device).run(topk_ids, stream)
+
+
+def permute(input: torch.Tensor, restore_token_order: torch.Tensor, stream=None) -> torch.Tensor:
+    N = restore_token_order.numel()
+    out = torch.empty((N, input.shape[1]), dtype=torch.bfloat16, device=input.device)
+    moe_permute(out, input, restore_token_order, stream)
+    return out
 
 
 def finalize(down: torch.Tensor, restore_order: torch.Tensor, router_weight: torch.Tensor,

@@ -23,10 +23,10 @@ constexpr int kFinThreads = 128;
 constexpr int kChunkUnroll = 2;
 
 struct FinArgs {
-  uint4* out;          // [T, H8] 16-byte chunks
-  const uint4* down;   // [N, H8]
+  void* out;           // [T, H] bf16 or fp32
+  const uint4* down;   // [N, H8] 16-byte chunks of 8 bf16
   const uint32_t* restore;
-  const float* weight;
+  const void* weight;  // [T, K] fp32 or bf16
   int64_t T;
   int K;
   int64_t H8;  // hidden / 8
@@ -50,18 +50,37 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4
   }
 }
 
-__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
-  uint32_t r[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-    r[j] = *reinterpret_cast<uint32_t*>(&p);
+// Router weight k of token t as fp32 (a bf16 weight widens exactly).
+template <typename WT>
+__device__ __forceinline__ float load_weight(const void* w, int64_t i) {
+  if constexpr (sizeof(WT) == 4) {
+    return __ldg(static_cast<const float*>(w) + i);
+  } else {
+    return __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(w) + i) << 16);
   }
-  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Chunk c (8 values) of output row t: bf16 rounded to nearest-even, or the fp32 sums.
+template <typename OT>
+__device__ __forceinline__ void store_chunk(void* out, int64_t t, int64_t H8, int64_t c,
+                                            const float (&acc)[8]) {
+  if constexpr (sizeof(OT) == 2) {
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      r[j] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    __stcs(static_cast<uint4*>(out) + t * H8 + c, make_uint4(r[0], r[1], r[2], r[3]));
+  } else {
+    float4* o = static_cast<float4*>(out) + (t * H8 + c) * 2;
+    __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+  }
 }
 
 // K known at compile time: all K row loads of kChunkUnroll chunks in flight.
-template <int K>
+template <int K, typename WT, typename OT>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) {
   wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
@@ -73,9 +92,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) 
       const uint32_t r = __ldg(a.restore + t * K + k);
       ok[k] = r < a.N;
       row[k] = (int64_t)(ok[k] ? r : 0u) * a.H8;
-      w[k] = __ldg(a.weight + t * K + k);
+      w[k] = load_weight<WT>(a.weight, t * K + k);
     }
-    uint4* out_row = a.out + t * a.H8;
     for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kFinThreads * kChunkUnroll) {
       uint4 v[kChunkUnroll][K];
 #pragma unroll
@@ -92,17 +110,17 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) 
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < K; ++k) fma_bf16x8(acc, w[k], v[u][k]);
-        __stcs(out_row + c, pack_bf16x8(acc));
+        store_chunk<OT>(a.out, t, a.H8, c, acc);
       }
     }
   }
 }
 
 // Any K <= 32: one row load per step, chunks unrolled for some overlap.
+template <typename WT, typename OT>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinArgs a) {
   wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-    uint4* out_row = a.out + t * a.H8;
     for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kFinThreads * kChunkUnroll) {
       float acc[kChunkUnroll][8];
 #pragma unroll
@@ -111,7 +129,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
         for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
       for (int k = 0; k < a.K; ++k) {
         const uint32_t r = __ldg(a.restore + t * a.K + k);
-        const float w = __ldg(a.weight + t * a.K + k);
+        const float w = load_weight<WT>(a.weight, t * a.K + k);
         if (r >= a.N) continue;
         const uint4* src = a.down + (int64_t)r * a.H8;
         uint4 v[kChunkUnroll];
@@ -126,7 +144,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
 #pragma unroll
       for (int u = 0; u < kChunkUnroll; ++u) {
         const int64_t c = c0 + (int64_t)u * kFinThreads;
-        if (c < a.H8) __stcs(out_row + c, pack_bf16x8(acc[u]));
+        if (c < a.H8) store_chunk<OT>(a.out, t, a.H8, c, acc[u]);
       }
     }
   }
@@ -143,6 +161,58 @@ moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream) {
   return launch(k, grid, kFinThreads, 0, stream, a);
 }
 
+using bf16_t = unsigned short;
+
+// fp32 weights, bf16 output: every specialised K.
+moe_status_t dispatch_default(const FinArgs& a, cudaStream_t stream) {
+  switch (a.K) {
+    case 1: return launch_fin(finalize_kernel<1, float, bf16_t>, a, stream);
+    case 2: return launch_fin(finalize_kernel<2, float, bf16_t>, a, stream);
+    case 4: return launch_fin(finalize_kernel<4, float, bf16_t>, a, stream);
+    case 6: return launch_fin(finalize_kernel<6, float, bf16_t>, a, stream);
+    case 8: return launch_fin(finalize_kernel<8, float, bf16_t>, a, stream);
+    default: return launch_fin(finalize_kernel_any_k<float, bf16_t>, a, stream);
+  }
+}
+
+// Other dtype pairs: K = 2 and K = 8 specialised, the rest generic.
+template <typename WT, typename OT>
+moe_status_t dispatch_typed(const FinArgs& a, cudaStream_t stream) {
+  switch (a.K) {
+    case 2: return launch_fin(finalize_kernel<2, WT, OT>, a, stream);
+    case 8: return launch_fin(finalize_kernel<8, WT, OT>, a, stream);
+    default: return launch_fin(finalize_kernel_any_k<WT, OT>, a, stream);
+  }
+}
+
+// Shared argument checks; fills `a` on success.
+moe_status_t check_and_pack(void* output, size_t out_elem, const moe_bf16_t* down,
+                            const uint32_t* restore_order, const void* router_weight,
+                            size_t w_elem, int64_t T, int K, int64_t hidden, FinArgs* a) {
+  if (T < 0 || K < 1 || hidden < 0) return MOE_ERR_INVALID_ARG;
+  if (hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (K > MOE_MAX_EXPERTS_PER_TOK) return MOE_ERR_UNSUPPORTED;
+  if (T * (int64_t)K > (int64_t)0xFFFFFFFFu) return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || hidden == 0) return MOE_OK;
+  if (!output || !down || !restore_order || !router_weight) return MOE_ERR_NULL_PTR;
+  if (!aligned(output, 16) || !aligned(down, 16) || !aligned(restore_order, 4) ||
+      !aligned(router_weight, w_elem))
+    return MOE_ERR_MISALIGNED;
+  // output must not overlap down (the kernel reads down while writing output)
+  const uintptr_t o0 = (uintptr_t)output, o1 = o0 + (uintptr_t)(T * hidden * out_elem);
+  const uintptr_t d0 = (uintptr_t)down, d1 = d0 + (uintptr_t)(T * K * hidden * 2);
+  if (o0 < d1 && d0 < o1) return MOE_ERR_INVALID_ARG;
+  a->out = output;
+  a->down = reinterpret_cast<const uint4*>(down);
+  a->restore = restore_order;
+  a->weight = router_weight;
+  a->T = T;
+  a->K = K;
+  a->H8 = hidden / 8;
+  a->N = (uint32_t)(T * K);
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -151,37 +221,29 @@ extern "C" moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
                                      int64_t num_tokens, int32_t num_experts_per_token,
                                      int64_t hidden, cudaStream_t stream) {
   using namespace moe;
-  const int64_t T = num_tokens;
-  const int K = num_experts_per_token;
-  if (T < 0 || K < 1 || hidden < 0) return MOE_ERR_INVALID_ARG;
-  if (hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (K > MOE_MAX_EXPERTS_PER_TOK) return MOE_ERR_UNSUPPORTED;
-  if (T * (int64_t)K > (int64_t)0xFFFFFFFFu) return MOE_ERR_UNSUPPORTED;
-  if (T == 0 || hidden == 0) return MOE_OK;
-  if (!output || !down || !restore_order || !router_weight) return MOE_ERR_NULL_PTR;
-  if (!aligned(output, 16) || !aligned(down, 16) || !aligned(restore_order, 4) ||
-      !aligned(router_weight, 4))
-    return MOE_ERR_MISALIGNED;
-  // output must not overlap down (the kernel reads down while writing output)
-  const uintptr_t o0 = (uintptr_t)output, o1 = o0 + (uintptr_t)(T * hidden * 2);
-  const uintptr_t d0 = (uintptr_t)down, d1 = d0 + (uintptr_t)(T * K * hidden * 2);
-  if (o0 < d1 && d0 < o1) return MOE_ERR_INVALID_ARG;
-
   FinArgs a;
-  a.out = reinterpret_cast<uint4*>(output);
-  a.down = reinterpret_cast<const uint4*>(down);
-  a.restore = restore_order;
-  a.weight = router_weight;
-  a.T = T;
-  a.K = K;
-  a.H8 = hidden / 8;
-  a.N = (uint32_t)(T * K);
-  switch (K) {
-    case 1: return launch_fin(finalize_kernel<1>, a, stream);
-    case 2: return launch_fin(finalize_kernel<2>, a, stream);
-    case 4: return launch_fin(finalize_kernel<4>, a, stream);
-    case 6: return launch_fin(finalize_kernel<6>, a, stream);
-    case 8: return launch_fin(finalize_kernel<8>, a, stream);
-    default: return launch_fin(finalize_kernel_any_k, a, stream);
-  }
+  const moe_status_t st = check_and_pack(output, 2, down, restore_order, router_weight, 4,
+                                         num_tokens, num_experts_per_token, hidden, &a);
+  if (st != MOE_OK || num_tokens == 0 || hidden == 0) return st;
+  return dispatch_default(a, stream);
+}
+
+extern "C" moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype,
+                                        const moe_bf16_t* down, const uint32_t* restore_order,
+                                        const void* router_weight, moe_dtype_t weight_dtype,
+                                        int64_t num_tokens, int32_t num_experts_per_token,
+                                        int64_t hidden, cudaStream_t stream) {
+  using namespace moe;
+  const bool out_f32 = output_dtype == MOE_DTYPE_F32, w_f32 = weight_dtype == MOE_DTYPE_F32;
+  if ((output_dtype != MOE_DTYPE_BF16 && !out_f32) || (weight_dtype != MOE_DTYPE_BF16 && !w_f32))
+    return MOE_ERR_UNSUPPORTED;
+  FinArgs a;
+  const moe_status_t st = check_and_pack(output, out_f32 ? 4 : 2, down, restore_order,
+                                         router_weight, w_f32 ? 4 : 2, num_tokens,
+                                         num_experts_per_token, hidden, &a);
+  if (st != MOE_OK || num_tokens == 0 || hidden == 0) return st;
+  if (w_f32 && !out_f32) return dispatch_default(a, stream);
+  if (w_f32 && out_f32) return dispatch_typed<float, float>(a, stream);
+  if (!w_f32 && !out_f32) return dispatch_typed<bf16_t, bf16_t>(a, stream);
+  return dispatch_typed<bf16_t, float>(a, stream);
 }

@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import torch
 
-from .binding import IndexBuffers, moe_finalize, moe_route
+from .binding import IndexBuffers, moe_finalize, moe_permute, moe_route
 
 
 class RoutingPipeline:
@@ -40,6 +40,11 @@ class RoutingPipeline:
     def finalize(self, down, stream=None, output=None):
         moe_finalize(self.output if output is None else output, down,
                      self.index.restore_token_order, self.expert_weights, stream)
+
+    def permute(self, x, out, stream=None):
+        """Expert-contiguous token rows for the grouped matmul (after create_indices)."""
+        moe_permute(out, x, self.index.restore_token_order, stream)
+        return out
 
     def __call__(self, expert_scores, expert_bias, down, stream=None) -> torch.Tensor:
         self.route(expert_scores, expert_bias, stream)

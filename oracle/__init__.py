@@ -48,8 +48,9 @@ def _open(path: str):
     lib.oracle_finalize.argtypes = [vp, vp, vp, i64, i32, i64, vp]
     lib.oracle_finalize_tokens.argtypes = [vp, vp, vp, i64, i32, i64, vp, i64, vp]
     lib.oracle_finalize_f64.argtypes = [vp, vp, vp, i64, i32, i64, vp]
+    lib.oracle_permute.argtypes = [vp, vp, i64, i32, i64, vp]
     for f in (lib.oracle_route, lib.oracle_create_indices, lib.oracle_finalize,
-              lib.oracle_finalize_tokens, lib.oracle_finalize_f64):
+              lib.oracle_finalize_tokens, lib.oracle_finalize_f64, lib.oracle_permute):
         f.restype = ctypes.c_int
     return lib
 
@@ -147,4 +148,15 @@ def finalize_f64(down_bf16_bits, restore, w, T: int, K: int, H: int):
     out = np.empty((T, H), dtype=np.float64)
     rc = _load().oracle_finalize_f64(dp, rp, wp, T, K, H, out.ctypes.data)
     _check(rc, "oracle_finalize_f64")
+    return out
+
+
+def permute(input_bf16_bits, token_expert_order, K: int):
+    """Expert-contiguous token rows [T*K, H] (bf16 bit patterns)."""
+    x, xp = _c(input_bf16_bits, np.uint16)
+    teo, tp = _c(token_expert_order, np.uint32)
+    T, H = x.shape
+    out = np.empty((T * K, H), dtype=np.uint16)
+    rc = _load().oracle_permute(xp, tp, T, K, H, out.ctypes.data)
+    _check(rc, "oracle_permute")
     return out

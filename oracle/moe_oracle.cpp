@@ -198,3 +198,20 @@ extern "C" int oracle_finalize_f64(const uint16_t* down, const uint32_t* restore
   }
   return ORACLE_OK;
 }
+
+// moe_create_indices, description paragraph: slots are grouped by expert so
+// that downstream kernels such as the grouped matmul process each expert's
+// tokens contiguously. Row p of that expert-contiguous input is the row of the
+// token owning slot token_expert_order[p] (slot i = t*K + k belongs to t).
+extern "C" int oracle_permute(const uint16_t* input, const uint32_t* token_expert_order,
+                              int64_t T, int32_t K, int64_t H, uint16_t* out) {
+  if (T < 0 || K <= 0 || H < 0) return ORACLE_ERR_ARG;
+  const int64_t N = T * K;
+  for (int64_t p = 0; p < N; ++p) {
+    const int64_t slot = token_expert_order[p];
+    if (slot >= N) return ORACLE_ERR_DATA;
+    const int64_t t = slot / K;
+    for (int64_t h = 0; h < H; ++h) out[p * H + h] = input[t * H + h];
+  }
+  return ORACLE_OK;
+}

@@ -15,6 +15,8 @@
  *     expert_usage_stats, topk_ids).
  *   - "moe_finalize": description paragraph; Args (output, down,
  *     restore_order, router_weight).
+ *   - the expert-contiguous token rows that the grouped matmul consumes
+ *     ("moe_create_indices", description paragraph).
  *
  * Readings where the pages are silent (each is listed with its reason in the
  * design notes of this repository):
@@ -77,6 +79,11 @@ int oracle_finalize(const uint16_t* down, const uint32_t* restore, const float* 
 int oracle_finalize_tokens(const uint16_t* down, const uint32_t* restore, const float* w,
                            int64_t T, int32_t K, int64_t H, const int64_t* tokens,
                            int64_t n_sel, float* out);
+
+/* Expert-contiguous token rows: out [T*K, H] row p = input row token_expert_order[p] / K.
+ * input [T, H] and out hold bf16 bit patterns. */
+int oracle_permute(const uint16_t* input, const uint32_t* token_expert_order, int64_t T, int32_t K,
+                   int64_t H, uint16_t* out);
 
 /* fp64 accumulation of the same sum (bounds the fp32 oracle's own rounding). */
 int oracle_finalize_f64(const uint16_t* down, const uint32_t* restore, const float* w, int64_t T,

@@ -25,6 +25,7 @@ _LIB_PATH = os.path.join(_HERE, "libsynth.so")
 TENSOR_SCORES = 1
 TENSOR_BIAS = 2
 TENSOR_DOWN = 3
+TENSOR_INPUT = 4
 
 
 def build(force: bool = False) -> str:
@@ -195,4 +196,16 @@ def make_down(cfg: MoeConfig, first_row: int = 0, n_rows: int | None = None,
                          threads=threads)
         return None
     return normal_bf16(cfg.seed, TENSOR_DOWN, n * cfg.H, first=first_row * cfg.H,
+                       threads=threads).reshape(n, cfg.H)
+
+
+def make_input(cfg: MoeConfig, first_row: int = 0, n_rows: int | None = None,
+               out_ptr: int | None = None, threads: int = 0):
+    """bf16 N(0,1) token rows [n_rows, H] (the permute's input) as uint16 bit patterns."""
+    n = cfg.T - first_row if n_rows is None else n_rows
+    if out_ptr is not None:
+        normal_bf16_into(out_ptr, cfg.seed, TENSOR_INPUT, n * cfg.H, first=first_row * cfg.H,
+                         threads=threads)
+        return None
+    return normal_bf16(cfg.seed, TENSOR_INPUT, n * cfg.H, first=first_row * cfg.H,
                        threads=threads).reshape(n, cfg.H)

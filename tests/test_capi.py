@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
          "moe_create_indices", "moe_finalize", "moe_read_device_status",
-         "moe_create_indices_no_alloc"])
+         "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -101,6 +101,29 @@ def test_finalize_host_validation(lib):
     assert f(p[0] + 8, *p[1:], 4, 2, 64, None) == 3
     assert f(p[0], p[0], p[2], p[3], 4, 2, 64, None) == 2   # output overlaps down
     assert f(None, None, None, None, 0, 2, 64, None) == 0   # T = 0
+
+
+def test_finalize_ex_host_validation(lib):
+    f = lib.moe_finalize_ex
+    o, d, r, w = FAKE, FAKE + 0x1000000, FAKE + 0x2000000, FAKE + 0x3000000
+    assert f(o, 2, d, r, w, 1, 4, 2, 64, None) == 4       # unknown output dtype
+    assert f(o, 0, d, r, w, 7, 4, 2, 64, None) == 4       # unknown weight dtype
+    assert f(o, 1, d, r, w + 2, 1, 4, 2, 64, None) == 3   # fp32 weights need 4-byte alignment
+    assert f(o, 1, d, r, w + 2, 0, 0, 2, 64, None) == 0   # T = 0
+    assert f(o, 1, o, r, w, 0, 4, 2, 64, None) == 2       # output overlaps down
+    assert f(o + 8, 1, d, r, w, 0, 4, 2, 64, None) == 3
+
+
+def test_permute_host_validation(lib):
+    f = lib.moe_permute
+    p = (FAKE, FAKE + 0x1000000, FAKE + 0x2000000)
+    assert f(*p, 4, 2, 60, None) == 4          # hidden % 8
+    assert f(*p, 4, 0, 64, None) == 2
+    assert f(*p, 4, 33, 64, None) == 4
+    assert f(None, *p[1:], 4, 2, 64, None) == 1
+    assert f(p[0] + 8, *p[1:], 4, 2, 64, None) == 3
+    assert f(p[0], p[0], p[2], 4, 2, 64, None) == 2   # permuted overlaps input
+    assert f(None, None, None, 0, 2, 64, None) == 0   # T = 0
 
 
 def test_device_status_host_validation(lib):

@@ -126,3 +126,47 @@ def test_deterministic():
     a = gpu_finalize(down, idx["restore_token_order"], w)
     b = gpu_finalize(down, idx["restore_token_order"], w)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("w_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [2, 3, 8])
+def test_finalize_ex_dtypes(w_dtype, out_dtype, K):
+    """moe_finalize page, Parameters weight_type / out_type: bf16 weights widen
+    exactly to fp32; an fp32 output is the oracle's fp32 sum bit for bit."""
+    import moe_token_routing_gb300 as moe
+    T, H = 211, 1032
+    down, restore, w = _case(T, K, H, K + 77)
+    if w_dtype == "bf16":
+        w_bits = f32_to_bf16_bits(w)
+        w_ref = bits_to_f32(w_bits).reshape(T, K)
+        w_dev = torch.from_numpy(w_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        w_ref = w
+        w_dev = torch.from_numpy(w).cuda()
+    ref = oracle.finalize(down, restore, w_ref, T, K, H)
+    tdt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    out = torch.empty((T, H), dtype=tdt, device="cuda")
+    r = torch.from_numpy(restore.view(np.int32)).cuda()
+    moe.moe_finalize_ex(out, to_dev_bf16(down), r, w_dev)
+    torch.cuda.synchronize()
+    if out_dtype == "f32":
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    else:
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert finalize_tolerance_ok(got, ref).all()
+        assert np.array_equal(got, f32_to_bf16_bits(ref))
+
+
+def test_finalize_ex_default_types_match_finalize():
+    import moe_token_routing_gb300 as moe
+    cfg, _, _, _, w, idx = workload("tiny")
+    down = workload_down("tiny")
+    r = torch.from_numpy(idx["restore_token_order"].view(np.int32)).cuda()
+    d = to_dev_bf16(down)
+    wd = torch.from_numpy(w).cuda()
+    a = moe.finalize(d, r, wd)
+    b = torch.empty_like(a)
+    moe.moe_finalize_ex(b, d, r, wd)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_finalize as tf
 import test_oracle_index as ti
+import test_oracle_permute as tp
 import test_oracle_route as tr
 
 ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
@@ -53,6 +54,9 @@ MUTANTS = {
     "finalize weight indexed k-major": (
         "acc = std::fma(w[t * K + k], bf16", "acc = std::fma(w[k * T + t], bf16"),
     "finalize reads down transposed": ("down[row * H + h]), acc)", "down[h * T * K + row]), acc)"),
+    "permute takes slot modulo K": ("const int64_t t = slot / K;", "const int64_t t = slot % K;"),
+    "permute copies the slot's row": ("out[p * H + h] = input[t * H + h];",
+                                      "out[p * H + h] = input[(p / K) * H + h];"),
 }
 
 
@@ -75,6 +79,9 @@ def _pins():
         lambda: tf.test_library_gather_weighted_sum(33, 8, 256),
         lambda: tf.test_library_gather_weighted_sum(17, 3, 72),
         tf.test_tiny_workload_chain,
+        tp.test_golden_fixture,
+        lambda: tp.test_library_gather(64, 4, 24),
+        lambda: tp.test_round_trip_through_finalize(2),
     ]
 
 
