@@ -61,6 +61,8 @@ typedef enum {
 #define MOE_MAX_EXPERTS 1024       /* n_routed_experts / n_experts */
 #define MOE_MAX_GROUPS 32          /* n_groups */
 #define MOE_MAX_EXPERTS_PER_TOK 32 /* n_experts_per_tok / num_experts_per_token */
+/* Row granularity of the per-expert scale blocks reported through scales_offset_p. */
+#define MOE_SCALES_ROW_ALIGNMENT 128
 
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status_t status);
@@ -97,6 +99,35 @@ moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
                        int32_t n_groups, int32_t topk_group, int32_t norm_weights,
                        float routed_scaling_factor, cudaStream_t stream);
 
+/* Score loaders of moe_route_ex (the page's scores_input_fn). */
+typedef enum {
+  MOE_SCORES_AS_GIVEN = 0, /* the score is the loaded value (moe_route) */
+  MOE_SCORES_SIGMOID = 1   /* the score is sigmoid(loaded logit) */
+} moe_score_fn_t;
+
+/*
+ * moe_route_ex -- moe_route with a fused score loader.
+ * Page "group_limited_router_kernel": Parameters scores_input_fn (an optional
+ * loader of the score of a (token, expert) pair; without it scores load from
+ * expert_scores).
+ *
+ * With MOE_SCORES_SIGMOID, expert_scores holds gate logits x and every score
+ * (for selection and for the weights) is sigmoid(x) = 1 / (1 + exp(-x)) in
+ * fp32, computed as the load happens, so the activated [T, E] tensor is never
+ * written. exp is the library's own: x clamped to [-87, 88], Cody-Waite
+ * reduction by ln2 (head 0.693145751953125, tail 1.42860682030941723e-6),
+ * degree-7 Taylor polynomial in Horner form with fused multiply-adds, times
+ * 2^n; within a few ulp of the true value, and reproducible bit for bit.
+ * Everything else is as in moe_route. An unknown score_fn returns
+ * MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_route_ex(int32_t* expert_indices, float* expert_weights,
+                          const float* expert_scores, const float* expert_bias,
+                          int64_t num_tokens, int32_t n_routed_experts, int32_t n_experts_per_tok,
+                          int32_t n_groups, int32_t topk_group, int32_t norm_weights,
+                          float routed_scaling_factor, moe_score_fn_t score_fn,
+                          cudaStream_t stream);
+
 /*
  * Workspace bytes that moe_create_indices needs for num_slots slots and
  * n_experts experts (always >= 256). Host-only; never fails (returns 0 for
@@ -126,7 +157,13 @@ size_t moe_create_indices_workspace_size(int64_t num_slots, int32_t n_experts);
  * workspace: device buffer of at least moe_create_indices_workspace_size()
  *   bytes, 256-byte aligned, caller-owned; its first 4 bytes receive the
  *   device status word. Calls sharing one workspace must not overlap.
- * scales_offset_p must be NULL (block-scaled offsets are not provided).
+ * scales_offset_p (optional, may be NULL) [E+1] uint32 out: the aligned scale
+ *   offsets for an FP8/block-scaled grouped matmul. The page does not give the
+ *   alignment; here every active expert's rows are padded to a multiple of
+ *   MOE_SCALES_ROW_ALIGNMENT, the row granularity of block-scaled tensor-core
+ *   scale-factor layouts: entry j < A = sum over active experts j' < j of
+ *   ceil(count_j' / 128) * 128, entries A .. E = that padded total. Requires
+ *   N + 127 * E < 2^32 (else MOE_ERR_UNSUPPORTED).
  * Requirements: 0 <= N < 2^32 - 1; 1 <= E <= MOE_MAX_EXPERTS; 4-byte aligned
  * buffers. Out-of-range ids set MOE_DEVICE_STATUS_BAD_EXPERT_ID, are left out
  * of every output count and leave the contents of the outputs unspecified.

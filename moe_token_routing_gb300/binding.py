@@ -26,7 +26,8 @@ DEVICE_STATUS_BAD_EXPERT_ID = 0x1
 # Entry points declared in include/moe_routing.h.
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
                     "moe_create_indices", "moe_finalize", "moe_read_device_status",
-                    "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex")
+                    "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex",
+                    "moe_route_ex")
 
 
 class MoeError(RuntimeError):
@@ -69,6 +70,9 @@ def load_library(path: str = LIB_PATH):
     lib.moe_permute.restype = ctypes.c_int
     lib.moe_finalize_ex.argtypes = [vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, i64, i32, i64, vp]
     lib.moe_finalize_ex.restype = ctypes.c_int
+    lib.moe_route_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, ctypes.c_int,
+                                 vp]
+    lib.moe_route_ex.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -115,6 +119,28 @@ def moe_route(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
                                   int(bool(norm_weights)), float(routed_scaling_factor),
                                   _stream(stream))
     _check("moe_route", rc)
+
+
+SCORES_AS_GIVEN = 0
+SCORES_SIGMOID = 1
+
+
+def moe_route_ex(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
+                 expert_scores: torch.Tensor, expert_bias: torch.Tensor, n_groups: int,
+                 topk_group: int, norm_weights: bool, routed_scaling_factor: float,
+                 score_fn: int = SCORES_SIGMOID, stream=None) -> None:
+    """moe_route with a fused score loader; with SCORES_SIGMOID expert_scores
+    holds gate logits and the scores are their sigmoid."""
+    T, E = expert_scores.shape
+    K = expert_indices.shape[1] if expert_indices.dim() == 2 else 0
+    args = (_dev(expert_indices, "expert_indices", torch.int32, (T, K)),
+            _dev(expert_weights, "expert_weights", torch.float32, (T, K)),
+            _dev(expert_scores, "expert_scores", torch.float32),
+            _dev(expert_bias, "expert_bias", torch.float32, (E,)))
+    rc = load_library().moe_route_ex(*args, T, E, K, int(n_groups), int(topk_group),
+                                     int(bool(norm_weights)), float(routed_scaling_factor),
+                                     int(score_fn), _stream(stream))
+    _check("moe_route_ex", rc)
 
 
 def moe_create_indices_workspace_size(num_slots: int, n_experts: int) -> int:

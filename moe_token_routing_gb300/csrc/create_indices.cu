@@ -38,6 +38,7 @@ constexpr int kSlotsPerWarp = 32 * kStepsPerWarp;
 constexpr int kSlotsPerCta = kIdxWarps * kSlotsPerWarp;  // 2048
 constexpr int kScanThreads = 1024;
 constexpr size_t kHeaderBytes = 256;
+constexpr uint32_t kScaleRowAlign = MOE_SCALES_ROW_ALIGNMENT;
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -74,6 +75,7 @@ struct IdxArgs {
   uint32_t* status;  // workspace word 0
   uint32_t* flags;   // [num_blocks]
   uint32_t* counts;  // [E][row]; the scan kernel, when used, overwrites it with bases
+  uint32_t* scales_offset;  // optional [E+1]: 128-row aligned per-expert offsets
   uint32_t N;
   int E;
   int num_blocks;
@@ -132,30 +134,36 @@ __device__ uint32_t block_max(uint32_t v, uint32_t* warp_tmp) {
 }
 
 // Given per-expert totals tot[0..E) in shared memory: writes the compact CSR,
-// expert_ids and usage stats, and turns tot[] into each expert's start offset.
-// `act` is E words of shared scratch.
-__device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act,
+// expert_ids and usage stats (and, if requested, the 128-row aligned scale
+// offsets), and turns tot[] into each expert's start offset. `act` and `pad`
+// are E words of shared scratch each.
+__device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act, uint32_t* pad,
                                   uint32_t* warp_tmp, bool write = true) {
+  const bool want_scales = a.scales_offset != nullptr;
   uint32_t local_max = 0;
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
     act[e] = tot[e] > 0u;
+    if (want_scales) pad[e] = (tot[e] + (kScaleRowAlign - 1)) / kScaleRowAlign * kScaleRowAlign;
     local_max = max(local_max, tot[e]);
   }
   __syncthreads();
   const uint32_t max_count = block_max(local_max, warp_tmp);
   const uint32_t active = block_exclusive_scan(act, a.E, warp_tmp);
   block_exclusive_scan(tot, a.E, warp_tmp);  // tot[e] := start of expert e
+  const uint32_t padded_total = want_scales ? block_exclusive_scan(pad, a.E, warp_tmp) : 0u;
   if (!write) return;
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
     const bool is_active = (e + 1 < a.E ? act[e + 1] : active) != act[e];
     if (is_active) {
       a.expert_ids[act[e]] = e;
       a.expert_start_indices[act[e]] = tot[e];
+      if (want_scales) a.scales_offset[act[e]] = pad[e];
     }
   }
   for (int j = (int)active + threadIdx.x; j <= a.E; j += blockDim.x) {
     a.expert_start_indices[j] = a.N;
     if (j < a.E) a.expert_ids[j] = -1;
+    if (want_scales) a.scales_offset[j] = padded_total;
   }
   if (threadIdx.x == 0) {
     a.stats[0] = max_count;
@@ -214,6 +222,7 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
   uint32_t* part = smem;                      // [P][E] partial sums per block range
   uint32_t* tot = part + kScanThreads;        // [E]
   uint32_t* act = tot + MOE_MAX_EXPERTS;      // [E]
+  uint32_t* pad = act + MOE_MAX_EXPERTS;      // [E]
   __shared__ uint32_t warp_tmp[32];
   wait_for_prior_grid();
 
@@ -239,7 +248,7 @@ __global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a)
     tot[threadIdx.x] = run;
   }
   __syncthreads();
-  emit_expert_table(a, tot, act, warp_tmp);
+  emit_expert_table(a, tot, act, pad, warp_tmp);
   __syncthreads();
   if (worker) {
     uint32_t base = tot[e] + part[p * E + e];
@@ -274,6 +283,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
   uint32_t* s_act = s_base + a.E;               // [E]
   uint32_t* s_pre = s_act + a.E;                // [E]
+  uint32_t* s_pad = s_pre + a.E;                // [E]
   __shared__ uint32_t warp_tmp[32];
   __shared__ uint32_t s_flags;
   wait_for_prior_grid();
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
       s_base[e] = t;
     }
     __syncthreads();
-    emit_expert_table(a, s_base, s_act, warp_tmp);
+    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
   } else if constexpr (kBases == kBasesFromCounts) {
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     }
     if (threadIdx.x == 0) s_flags = 0;
     __syncthreads();
-    emit_expert_table(a, s_base, s_act, warp_tmp, b == 0);  // s_base[e] := start(e)
+    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp, b == 0);  // s_base[e] := start(e)
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
     if (b == 0) {
       uint32_t f = 0;
@@ -369,7 +379,17 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
 }
 
 moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream) {
-  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 3) * a.E;
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 4) * a.E;
+  if (scatter_smem > 40 * 1024) {  // large E: opt in above the default 48 KB block limit
+    const int bytes = (int)scatter_smem;
+    if (cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromCounts>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromScan>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (L.num_blocks <= 1) {
     return launch(idx_scatter_kernel<kBasesSingleCta>, 1, kIdxThreads, scatter_smem, stream, a);
   }
@@ -379,7 +399,7 @@ moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream
   if (L.row * a.E <= kMaxSharedCountWords)
     return launch(idx_scatter_kernel<kBasesFromCounts>, a.num_blocks, kIdxThreads, scatter_smem,
                   stream, a);
-  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 2 * MOE_MAX_EXPERTS);
+  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 3 * MOE_MAX_EXPERTS);
   st = launch(idx_scan_kernel, 1, kScanThreads, scan_smem, stream, a);
   if (st != MOE_OK) return st;
   return launch(idx_scatter_kernel<kBasesFromScan>, a.num_blocks, kIdxThreads, scatter_smem,
@@ -406,7 +426,9 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   const int E = n_experts;
   if (N < 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (E > MOE_MAX_EXPERTS || N > (int64_t)0xFFFFFFFEu) return MOE_ERR_UNSUPPORTED;
-  if (scales_offset_p != nullptr) return MOE_ERR_UNSUPPORTED;
+  if (scales_offset_p != nullptr &&
+      N + (int64_t)(kScaleRowAlign - 1) * E > (int64_t)0xFFFFFFFFu)
+    return MOE_ERR_UNSUPPORTED;
   if (!expert_start_indices || !expert_ids || !expert_usage_stats) return MOE_ERR_NULL_PTR;
   if (N > 0 && (!token_expert_order || !restore_token_order || !topk_ids))
     return MOE_ERR_NULL_PTR;
@@ -415,7 +437,7 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
   if (!aligned(token_expert_order, 4) || !aligned(expert_start_indices, 4) ||
       !aligned(restore_token_order, 4) || !aligned(expert_ids, 4) ||
-      !aligned(expert_usage_stats, 4) || !aligned(topk_ids, 4))
+      !aligned(expert_usage_stats, 4) || !aligned(topk_ids, 4) || !aligned(scales_offset_p, 4))
     return MOE_ERR_MISALIGNED;
 
   char* ws = static_cast<char*>(workspace);
@@ -426,6 +448,7 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   a.restore_token_order = restore_token_order;
   a.expert_ids = expert_ids;
   a.stats = expert_usage_stats;
+  a.scales_offset = scales_offset_p;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
@@ -515,6 +538,7 @@ extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order
   a.restore_token_order = restore_token_order;
   a.expert_ids = expert_ids;
   a.stats = expert_usage_stats;
+  a.scales_offset = nullptr;
   a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(ws);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);

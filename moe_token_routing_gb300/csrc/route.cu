@@ -46,7 +46,37 @@ struct RouteArgs {
   float scale;
   int group_mode;
   int seg_lanes;  // lanes per group in kGroupsSegment
+  int score_fn;   // moe_score_fn_t applied to every loaded score
 };
+
+// exp(x) in fp32 by Cody-Waite range reduction (W. J. Cody and W. Waite,
+// "Software Manual for the Elementary Functions", 1980): x = n ln2 + r with
+// |r| <= ln2/2, ln2 split into a head with 12 trailing zero bits (so n*head is
+// exact) and a tail; exp(r) by its Taylor series to degree 7 in Horner form
+// with fused multiply-adds; 2^n assembled from exponent bits. x is clamped to
+// [-87, 88] so that 2^n is a normal float. Every step is a correctly rounded
+// fp32 operation, so the result is reproducible bit for bit.
+__device__ __forceinline__ float score_exp_f32(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 1.44269504088896341f));
+  float r = __fmaf_rn(-n, 0.693145751953125f, x);
+  r = __fmaf_rn(-n, 1.42860682030941723e-6f, r);
+  float p = 1.98412698412698413e-4f;             // 1/7!
+  p = __fmaf_rn(p, r, 1.38888888888888889e-3f);  // 1/6!
+  p = __fmaf_rn(p, r, 8.33333333333333333e-3f);  // 1/5!
+  p = __fmaf_rn(p, r, 4.16666666666666667e-2f);  // 1/4!
+  p = __fmaf_rn(p, r, 1.66666666666666667e-1f);  // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+// The page's scores_input_fn: the score of (token, expert) from the loaded value.
+__device__ __forceinline__ float apply_score_fn(int fn, float x) {
+  if (fn == MOE_SCORES_SIGMOID) return __fdiv_rn(1.0f, __fadd_rn(1.0f, score_exp_f32(-x)));
+  return x;
+}
 
 // Running top-2 of a stream of values (multiset: equal values both count).
 __device__ __forceinline__ void top2_push(float& t1, float& t2, float x) {
@@ -151,6 +181,10 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
 #pragma unroll
     for (int c = 0; c < C; ++c) s[c] = s_next[c];
     if (t + stride < a.T) load_lane_scores<C, kVec>(a, t + stride, e0, valid, s_next);
+    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] = apply_score_fn(a.score_fn, s[c]);
+    }
 
     float b[C];
 #pragma unroll
@@ -278,7 +312,7 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
 
     // ---- weights: unbiased score, optional normalisation, scaling ----
     const float* row = a.scores + t * a.E;
-    float w = (lane < a.K) ? __ldg(row + my_id) : 0.0f;
+    float w = (lane < a.K) ? apply_score_fn(a.score_fn, __ldg(row + my_id)) : 0.0f;
     if (a.norm) {
       float sum = 0.0f;
 #pragma unroll 8
@@ -326,6 +360,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const Route
     } else {
 #pragma unroll
       for (int e = 0; e < EP; ++e) s[e] = ((valid >> e) & 1u) ? __ldg(row + e) : 0.0f;
+    }
+    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+#pragma unroll
+      for (int e = 0; e < EP; ++e) s[e] = apply_score_fn(a.score_fn, s[e]);
     }
     float b[EP];
 #pragma unroll
@@ -440,13 +478,14 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 }  // namespace
 }  // namespace moe
 
-extern "C" moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
-                                  const float* expert_scores, const float* expert_bias,
-                                  int64_t num_tokens, int32_t n_routed_experts,
-                                  int32_t n_experts_per_tok, int32_t n_groups,
-                                  int32_t topk_group, int32_t norm_weights,
-                                  float routed_scaling_factor, cudaStream_t stream) {
-  using namespace moe;
+namespace moe {
+namespace {
+
+moe_status_t route_impl(int32_t* expert_indices, float* expert_weights,
+                        const float* expert_scores, const float* expert_bias, int64_t num_tokens,
+                        int32_t n_routed_experts, int32_t n_experts_per_tok, int32_t n_groups,
+                        int32_t topk_group, int32_t norm_weights, float routed_scaling_factor,
+                        int32_t score_fn, cudaStream_t stream) {
   const int E = n_routed_experts, K = n_experts_per_tok, G = n_groups, M = topk_group;
   if (num_tokens < 0 || E < 1 || G < 1 || M < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (E % G != 0 || M > G) return MOE_ERR_INVALID_ARG;
@@ -477,6 +516,7 @@ extern "C" moe_status_t moe_route(int32_t* expert_indices, float* expert_weights
   a.scale = routed_scaling_factor;
   a.group_mode = kGroupsAllKept;
   a.seg_lanes = 1;
+  a.score_fn = score_fn;
   const bool vec = (E % 4 == 0) && aligned(expert_scores, 16);
 
   if (E <= 32) {
@@ -500,4 +540,32 @@ extern "C" moe_status_t moe_route(int32_t* expert_indices, float* expert_weights
     case 16: return launch_warp_path<16>(a, vec, stream);
     default: return launch_warp_path<32>(a, vec, stream);
   }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
+                                  const float* expert_scores, const float* expert_bias,
+                                  int64_t num_tokens, int32_t n_routed_experts,
+                                  int32_t n_experts_per_tok, int32_t n_groups,
+                                  int32_t topk_group, int32_t norm_weights,
+                                  float routed_scaling_factor, cudaStream_t stream) {
+  return moe::route_impl(expert_indices, expert_weights, expert_scores, expert_bias, num_tokens,
+                         n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights,
+                         routed_scaling_factor, MOE_SCORES_AS_GIVEN, stream);
+}
+
+extern "C" moe_status_t moe_route_ex(int32_t* expert_indices, float* expert_weights,
+                                     const float* expert_scores, const float* expert_bias,
+                                     int64_t num_tokens, int32_t n_routed_experts,
+                                     int32_t n_experts_per_tok, int32_t n_groups,
+                                     int32_t topk_group, int32_t norm_weights,
+                                     float routed_scaling_factor, moe_score_fn_t score_fn,
+                                     cudaStream_t stream) {
+  if (score_fn != MOE_SCORES_AS_GIVEN && score_fn != MOE_SCORES_SIGMOID)
+    return MOE_ERR_UNSUPPORTED;
+  return moe::route_impl(expert_indices, expert_weights, expert_scores, expert_bias, num_tokens,
+                         n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights,
+                         routed_scaling_factor, score_fn, stream);
 }

@@ -49,8 +49,11 @@ def _open(path: str):
     lib.oracle_finalize_tokens.argtypes = [vp, vp, vp, i64, i32, i64, vp, i64, vp]
     lib.oracle_finalize_f64.argtypes = [vp, vp, vp, i64, i32, i64, vp]
     lib.oracle_permute.argtypes = [vp, vp, i64, i32, i64, vp]
+    lib.oracle_scales_offsets.argtypes = [vp, i64, i32, ctypes.c_uint32, vp]
+    lib.oracle_sigmoid.argtypes = [vp, i64, vp]
     for f in (lib.oracle_route, lib.oracle_create_indices, lib.oracle_finalize,
-              lib.oracle_finalize_tokens, lib.oracle_finalize_f64, lib.oracle_permute):
+              lib.oracle_finalize_tokens, lib.oracle_finalize_f64, lib.oracle_permute,
+              lib.oracle_scales_offsets, lib.oracle_sigmoid):
         f.restype = ctypes.c_int
     return lib
 
@@ -159,4 +162,21 @@ def permute(input_bf16_bits, token_expert_order, K: int):
     out = np.empty((T * K, H), dtype=np.uint16)
     rc = _load().oracle_permute(xp, tp, T, K, H, out.ctypes.data)
     _check(rc, "oracle_permute")
+    return out
+
+
+def scales_offsets(topk_ids, E: int, row_align: int = 128):
+    """Aligned per-expert scale offsets [E+1] (see moe_oracle.h)."""
+    ids, ip = _c(np.asarray(topk_ids).reshape(-1), np.int32)
+    out = np.empty(E + 1, dtype=np.uint32)
+    rc = _load().oracle_scales_offsets(ip, ids.size, E, row_align, out.ctypes.data)
+    _check(rc, "oracle_scales_offsets")
+    return out
+
+
+def sigmoid(x):
+    """fp32 sigmoid score loader (same shape as x)."""
+    a, ap = _c(x, np.float32)
+    out = np.empty_like(a)
+    _check(_load().oracle_sigmoid(ap, a.size, out.ctypes.data), "oracle_sigmoid")
     return out

@@ -18,7 +18,39 @@ float bf16_bits_to_float(uint16_t b) {
   return f;
 }
 
+// exp(x) for the sigmoid score loader, in fp32, following Cody and Waite's
+// range reduction ("Software Manual for the Elementary Functions", 1980):
+//   clamp x to [-87, 88];  n = round-to-nearest-even(x * log2(e));
+//   r = (x - n * ln2_head) - n * ln2_tail   (two fused multiply-adds; ln2_head
+//       = 0.693145751953125 has 12 trailing zero bits, ln2_tail = ln2 - head);
+//   exp(r) = sum_{k=0..7} r^k / k!   (Horner's rule, fused multiply-adds);
+//   exp(x) = exp(r) * 2^n.
+float exp_cody_waite(float x) {
+  x = std::fmin(std::fmax(x, -87.0f), 88.0f);
+  const float n = std::rint(x * 1.44269504088896341f);
+  float r = std::fma(-n, 0.693145751953125f, x);
+  r = std::fma(-n, 1.42860682030941723e-6f, r);
+  const float inv_fact[8] = {1.0f, 1.0f, 0.5f, 1.66666666666666667e-1f, 4.16666666666666667e-2f,
+                             8.33333333333333333e-3f, 1.38888888888888889e-3f,
+                             1.98412698412698413e-4f};
+  float p = inv_fact[7];
+  for (int k = 6; k >= 0; --k) p = std::fma(p, r, inv_fact[k]);
+  return p * std::ldexp(1.0f, static_cast<int>(n));
+}
+
 }  // namespace
+
+// group_limited_router_kernel, Parameters scores_input_fn: an optional loader
+// of each (token, expert) score; here the score of a gate logit x is its
+// sigmoid 1 / (1 + exp(-x)).
+extern "C" int oracle_sigmoid(const float* x, int64_t n, float* out) {
+  if (n < 0) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (std::isnan(x[i])) return ORACLE_ERR_NAN;
+    out[i] = 1.0f / (1.0f + exp_cody_waite(-x[i]));
+  }
+  return ORACLE_OK;
+}
 
 // group_limited_router_kernel, description paragraph: experts are split into
 // n_groups groups, the topk_group best groups are kept, and the
@@ -135,6 +167,29 @@ extern "C" int oracle_create_indices(const int32_t* topk_ids, int64_t N, int32_t
 
   expert_usage_stats[0] = max_count;
   expert_usage_stats[1] = active;
+  return ORACLE_OK;
+}
+
+// moe_create_indices, Args scales_offset_p: aligned scale offsets for an
+// FP8/block-scaled grouped matmul. Reading (the page gives no alignment): each
+// active expert's rows are padded to a multiple of row_align, and the offsets
+// are the running sums of the padded counts, in active-expert order.
+extern "C" int oracle_scales_offsets(const int32_t* topk_ids, int64_t N, int32_t E,
+                                     uint32_t row_align, uint32_t* out) {
+  if (N < 0 || E <= 0 || row_align == 0) return ORACLE_ERR_ARG;
+  std::vector<uint64_t> count(E, 0);
+  for (int64_t i = 0; i < N; ++i) {
+    if (topk_ids[i] < 0 || topk_ids[i] >= E) return ORACLE_ERR_DATA;
+    count[topk_ids[i]] += 1;
+  }
+  uint64_t offset = 0;
+  int32_t j = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    if (count[e] == 0) continue;
+    out[j++] = static_cast<uint32_t>(offset);
+    offset += (count[e] + row_align - 1) / row_align * row_align;
+  }
+  for (; j <= E; ++j) out[j] = static_cast<uint32_t>(offset);
   return ORACLE_OK;
 }
 

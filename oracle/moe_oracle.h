@@ -15,6 +15,8 @@
  *     expert_usage_stats, topk_ids).
  *   - "moe_finalize": description paragraph; Args (output, down,
  *     restore_order, router_weight).
+ *   - "group_limited_router_kernel", Parameters scores_input_fn: a sigmoid
+ *     score loader for gate logits;
  *   - the expert-contiguous token rows that the grouped matmul consumes
  *     ("moe_create_indices", description paragraph).
  *
@@ -56,6 +58,10 @@ extern "C" {
 #define ORACLE_ERR_NAN -2
 #define ORACLE_ERR_DATA -3
 
+/* Sigmoid score loader: out[i] = 1 / (1 + exp(-x[i])) in fp32, with exp by
+ * Cody-Waite reduction and a degree-7 Taylor polynomial (see the .cpp). */
+int oracle_sigmoid(const float* x, int64_t n, float* out);
+
 /* Router. scores [T,E] fp32 row-major, bias [E] fp32.
  * ids_out [T,K] int32, w_out [T,K] fp32. */
 int oracle_route(const float* scores, const float* bias, int64_t T, int32_t E, int32_t K,
@@ -69,6 +75,13 @@ int oracle_create_indices(const int32_t* topk_ids, int64_t N, int32_t E,
                           uint32_t* token_expert_order, uint32_t* expert_start_indices,
                           uint32_t* restore_token_order, int32_t* expert_ids,
                           uint32_t* expert_usage_stats);
+
+/* Aligned scale offsets of the active experts for a block-scaled grouped
+ * matmul: out [E+1], entry j < A = sum over active experts j' < j of the
+ * expert's slot count rounded up to a multiple of `row_align`; entries A..E =
+ * the padded total. */
+int oracle_scales_offsets(const int32_t* topk_ids, int64_t N, int32_t E, uint32_t row_align,
+                          uint32_t* out);
 
 /* Finalize, fp32 accumulation, result before bf16 rounding.
  * down [T*K, H] bf16 bit patterns, restore [T*K], w [T,K], out [T,H] fp32. */

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
          "moe_create_indices", "moe_finalize", "moe_read_device_status",
-         "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex"])
+         "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex", "moe_route_ex"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -75,11 +75,20 @@ def test_route_host_validation(lib):
     assert f(None, None, None, None, 0, 256, 8, 8, 4, 1, 1.0, None) == 0  # T = 0: nothing to do
 
 
+def test_route_ex_host_validation(lib):
+    f = lib.moe_route_ex
+    ok = (FAKE, FAKE, FAKE, FAKE)
+    assert f(*ok, 4, 256, 8, 8, 4, 1, 1.0, 7, None) == 4      # unknown score loader
+    assert f(*ok, 4, 256, 8, 7, 4, 1, 1.0, 1, None) == 2      # E % n_groups
+    assert f(None, None, None, None, 0, 256, 8, 8, 4, 1, 1.0, 1, None) == 0
+
+
 def test_create_indices_host_validation(lib):
     f = lib.moe_create_indices
     outs = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
     ws = lib.moe_create_indices_workspace_size(100000, 64)
-    assert f(*outs, 100000, 64, FAKE, ws, FAKE, None) == 4          # scales_offset_p given
+    # scale offsets would pass 2^32 (N + 127 * E): rejected before anything is enqueued
+    assert f(*outs, 0xFFFFFF00, 64, FAKE, ws, FAKE, None) == 4
     assert f(*outs, 100000, 64, FAKE, ws - 1, None, None) == 6      # workspace too small
     assert f(*outs, 100000, 64, None, ws, None, None) == 6          # no workspace
     assert f(*outs, 100000, 64, FAKE + 16, ws, None, None) == 3     # workspace alignment

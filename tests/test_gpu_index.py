@@ -109,3 +109,33 @@ def test_deterministic():
     b, _ = gpu_index(ids, cfg.E)
     for k in KEYS:
         assert np.array_equal(a[k], b[k])
+
+
+@pytest.mark.parametrize("N,E", [(1000, 16), (2048, 256), (131072, 256), (100003, 1000), (0, 8)])
+def test_scales_offsets(N, E):
+    """moe_create_indices page, Args scales_offset_p: 128-row aligned offsets
+    of the active experts (the alignment is this build's reading)."""
+    import moe_token_routing_gb300 as moe
+    rng = np.random.default_rng(N + E)
+    ids = rng.integers(0, E, size=N).astype(np.int32)
+    ids[: N // 3] = 0  # one heavy expert
+    t = torch.from_numpy(ids).cuda()
+    bufs = moe.IndexBuffers(N, E, "cuda")
+    scales = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    lib = moe.load_library()
+    rc = lib.moe_create_indices(bufs.token_expert_order.data_ptr() if N else None,
+                                bufs.expert_start_indices.data_ptr(),
+                                bufs.restore_token_order.data_ptr() if N else None,
+                                bufs.expert_ids.data_ptr(), bufs.expert_usage_stats.data_ptr(),
+                                t.data_ptr() if N else None, N, E, bufs.workspace.data_ptr(),
+                                bufs.workspace.numel(), scales.data_ptr(),
+                                torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), oracle.scales_offsets(ids, E))
+    ref = oracle.create_indices(ids, E)
+    for k in KEYS:
+        got = getattr(bufs, k).cpu().numpy()
+        if k != "expert_ids":
+            got = got.view(np.uint32)
+        assert np.array_equal(got, ref[k]), k

@@ -147,3 +147,43 @@ def test_deterministic():
     a = gpu_route(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
     b = gpu_route(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
+
+
+def gpu_route_sigmoid(logits, bias, K, G, M, norm, scale):
+    import moe_token_routing_gb300 as moe
+    s = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+    b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
+    T = logits.shape[0]
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route_ex(ids, w, s, b, G, M, norm, scale, moe.SCORES_SIGMOID)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_sigmoid_loader_on_workloads(name):
+    """Parameters scores_input_fn: routing gate logits with the fused sigmoid
+    equals routing the oracle's sigmoid of the same logits, bit for bit."""
+    cfg = synth.get_config(name)
+    logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
+    bias = synth.make_bias(cfg)
+    ids_ref, w_ref = oracle.route(oracle.sigmoid(logits), bias, cfg.K, cfg.G, cfg.M,
+                                  cfg.norm_weights, cfg.scale)
+    ids, w = gpu_route_sigmoid(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    assert np.array_equal(ids, ids_ref)
+    assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,G,M,K", [(8, 4, 2, 3), (16, 4, 2, 4), (96, 4, 2, 8), (256, 8, 4, 8),
+                                     (384, 1, 1, 8)])
+def test_sigmoid_loader_shapes_and_extremes(E, G, M, K):
+    rng = np.random.default_rng(E + K)
+    logits = (rng.standard_normal((300, E)) * 6).astype(np.float32)
+    logits[::7, ::3] = 120.0
+    logits[1::7, ::5] = -120.0
+    bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    ids_ref, w_ref = oracle.route(oracle.sigmoid(logits), bias, K, G, M, True, 2.5)
+    ids, w = gpu_route_sigmoid(logits, bias, K, G, M, True, 2.5)
+    assert np.array_equal(ids, ids_ref)
+    assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))

@@ -16,6 +16,8 @@ import test_oracle_finalize as tf
 import test_oracle_index as ti
 import test_oracle_permute as tp
 import test_oracle_route as tr
+import test_oracle_scales as tsc
+import test_oracle_sigmoid as tsg
 
 ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
 
@@ -54,6 +56,12 @@ MUTANTS = {
     "finalize weight indexed k-major": (
         "acc = std::fma(w[t * K + k], bf16", "acc = std::fma(w[k * T + t], bf16"),
     "finalize reads down transposed": ("down[row * H + h]), acc)", "down[h * T * K + row]), acc)"),
+    "scale offsets not rounded up": (
+        "offset += (count[e] + row_align - 1) / row_align * row_align;",
+        "offset += count[e] / row_align * row_align;"),
+    "sigmoid drops a Taylor term": ("for (int k = 6; k >= 0; --k) p = std::fma(p, r, inv_fact[k]);",
+                                    "for (int k = 6; k >= 1; --k) p = std::fma(p, r, inv_fact[k]);"),
+    "sigmoid without the ln2 tail": ("r = std::fma(-n, 1.42860682030941723e-6f, r);", "r = r;"),
     "permute takes slot modulo K": ("const int64_t t = slot / K;", "const int64_t t = slot % K;"),
     "permute copies the slot's row": ("out[p * H + h] = input[t * H + h];",
                                       "out[p * H + h] = input[(p / K) * H + h];"),
@@ -82,6 +90,9 @@ def _pins():
         tp.test_golden_fixture,
         lambda: tp.test_library_gather(64, 4, 24),
         lambda: tp.test_round_trip_through_finalize(2),
+        tsc.test_golden_fixture,
+        tsg.test_error_bound_on_a_grid,
+        tsg.test_special_values,
     ]
 
 
