@@ -3,7 +3,9 @@
 One step = the three stages over one batch of seeded synthetic input
 (default: the DeepSeek-V3-shaped prefill workload, T=16384 tokens, E=256
 experts in 8 groups, top-4 groups, K=8, H=7168), inputs resident in HBM,
-L2 flushed (a 256 MB write) before every step outside the timed events.
+L2 flushed before every step outside the timed events: a 256 MB write evicts
+everything, then a 256 MB read writes back the dirty lines the write left and
+leaves L2 holding only clean data that no step uses.
 
 Prints ONE JSON line. `value` is whole-job tokens/s from CUDA-event device
 time per step; `e2e` is the same metric through the host-buffer call
@@ -260,7 +262,8 @@ def config_dict(cfg):
             "hidden": cfg.H, "norm_weights": cfg.norm_weights,
             "routed_scaling_factor": cfg.scale, "scores": cfg.scores, "bias": cfg.bias,
             "down_dtype": "bf16", "weights_dtype": "f32", "output_dtype": "bf16",
-            "l2": "flushed before every step (256 MB write, outside the timed events)"}
+            "l2": "flushed before every step outside the timed events: 256 MB write, then "
+                  "256 MB read (so no dirty flush lines are written back inside the step)"}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -283,7 +286,13 @@ def run_gpu(args, cfg, rank, world, local_rank):
     d_d = down_h.to(dev)
     pipe = moe.RoutingPipeline(cfg.T, cfg.E, cfg.K, cfg.H, cfg.G, cfg.M, cfg.norm_weights,
                                cfg.scale, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
+
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -291,7 +300,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
             dist.barrier()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         pipe(s_d, b_d, d_d)
     torch.cuda.synchronize(dev)
 
@@ -306,7 +315,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.zero_()
+        flush_l2()
         e = ev[i]
         e[0].record(stream)
         pipe.route(s_d, b_d)
@@ -327,7 +336,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     ks = min(K, 200)
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ks)]
     for i in range(ks):
-        flush.zero_()
+        flush_l2()
         e = sev[i]
         e[0].record(stream)
         pipe.route(s_d, b_d)
@@ -357,7 +366,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     kp = min(K, 100)
     pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kp)]
     for i in range(kp):
-        flush.zero_()
+        flush_l2()
         pev[i][0].record(stream)
         pipe.permute(x_d, perm_out)
         pev[i][1].record(stream)
@@ -371,7 +380,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     ids_x = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device=dev)
     w_x = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=dev)
     for i in range(kp):
-        flush.zero_()
+        flush_l2()
         pev[i][0].record(stream)
         moe.moe_route_ex(ids_x, w_x, logits_d, b_d, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
                          moe.SCORES_SIGMOID)
