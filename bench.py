@@ -60,6 +60,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def index_launches(num_slots: int, n_experts: int) -> int:
+    """Kernels one moe_create_indices call launches: one CTA does everything for
+    N <= 2048 slots; otherwise count + scatter, plus a scan kernel when the
+    count matrix (experts x 2048-slot chunks, rows padded to 4) exceeds 32Ki words."""
+    chunks = -(-num_slots // 2048)
+    if chunks <= 1:
+        return 1
+    row = (chunks + 3) // 4 * 4
+    return 2 if row * n_experts <= 32 * 1024 else 3
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """Largest value of x over all ranks (the timing reduction; not on the data path)."""
     if world <= 1:
@@ -421,7 +432,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     route_mean = statistics.fmean(route_ms)
     fin_gbs = nbytes["finalize"] / (fin_mean * 1e-3) / 1e9
     route_gbs = nbytes["route"] / (route_mean * 1e-3) / 1e9
-    launches_per_step = 1 + (1 if cfg.N <= 2048 else 3) + 1
+    launches_per_step = 1 + index_launches(cfg.N, cfg.E) + 1
 
     cpu = None
     if not args.no_cpu_baseline:

@@ -61,3 +61,15 @@ def test_reference_arm_only_on_rank_zero(capsys):
         steps, warmup = 1, 0
     bench.run_reference(A, synth.get_config("tiny"), rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_index_launch_count_matches_library_rule():
+    """bench.py's launch count mirrors the index builder's dispatch."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.index_launches(0, 8) == 1
+    assert bench.index_launches(2048, 256) == 1
+    assert bench.index_launches(2049, 256) == 2
+    assert bench.index_launches(131072, 256) == 2     # 64 chunks x 256 experts = 16Ki words
+    assert bench.index_launches(100003, 1000) == 3    # 52 x 1000 words > 32Ki
+    assert bench.index_launches(262144, 8) == 2
