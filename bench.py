@@ -49,6 +49,9 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (profiling runs)")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--fused-index", action="store_true",
+                   help="time the fused moe_route_index launch in the steps instead of "
+                        "moe_route followed by moe_create_indices")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -295,8 +298,10 @@ def run_gpu(args, cfg, rank, world, local_rank):
     s_d = torch.from_numpy(scores).to(dev)
     b_d = torch.from_numpy(bias).to(dev)
     d_d = down_h.to(dev)
+    fused = args.fused_index
     pipe = moe.RoutingPipeline(cfg.T, cfg.E, cfg.K, cfg.H, cfg.G, cfg.M, cfg.norm_weights,
-                               cfg.scale, device=dev)
+                               cfg.scale, device=dev, fused=True)
+    pipe.fused = fused  # both paths stay available for the stage pass
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
@@ -317,7 +322,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
 
     K = args.steps
     # Timed region: events only at the step start, before finalize and at the
-    # step end, so the route -> create_indices launches chain back to back.
+    # step end, so the route -> create_indices launches (or the fused
+    # route_index launch) and finalize chain back to back.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(device_uuid(dev))
     sampler.start()
@@ -329,8 +335,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         flush_l2()
         e = ev[i]
         e[0].record(stream)
-        pipe.route(s_d, b_d)
-        pipe.create_indices()
+        pipe.route_and_index(s_d, b_d)
         e[1].record(stream)
         pipe.finalize(d_d)
         e[2].record(stream)
@@ -360,6 +365,19 @@ def run_gpu(args, cfg, rank, world, local_rank):
     route_ms = [e[0].elapsed_time(e[1]) for e in sev]
     index_ms = [e[1].elapsed_time(e[2]) for e in sev]
     fin_stage_ms = [e[2].elapsed_time(e[3]) for e in sev]
+    # the fused launch as a stage of its own
+    for i in range(ks):
+        flush_l2()
+        e = sev[i]
+        e[0].record(stream)
+        pipe.route_index(s_d, b_d)
+        e[1].record(stream)
+        pipe.finalize(d_d)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    fused_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    status_ok = (moe.moe_read_device_status(pipe.fused_workspace) == 0
+                 and moe.moe_read_device_status(pipe.index.workspace) == 0)
 
     # whole-job throughput: max over ranks of the mean step time
     worst_ms = max_over_ranks(mean_step, world, dev)
@@ -432,7 +450,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     route_mean = statistics.fmean(route_ms)
     fin_gbs = nbytes["finalize"] / (fin_mean * 1e-3) / 1e9
     route_gbs = nbytes["route"] / (route_mean * 1e-3) / 1e9
-    launches_per_step = 1 + index_launches(cfg.N, cfg.E) + 1
+    launches_per_step = (1 if fused else 1 + index_launches(cfg.N, cfg.E)) + 1
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -446,7 +464,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
         "ms_per_step": worst_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded)",
-        "config": config_dict(cfg),
+        "config": dict(config_dict(cfg), route_index="fused (moe_route_index, one launch)"
+                       if fused else "separate (moe_route, moe_create_indices)"),
         "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": fin_gbs, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": fin_gbs / peak,
                      "frac_vs_nominal_8tbs": fin_gbs / NOMINAL_HBM_GBS,
@@ -458,13 +477,16 @@ def run_gpu(args, cfg, rank, world, local_rank):
                             "frac_vs_nominal_8tbs": route_gbs / NOMINAL_HBM_GBS,
                             "algorithmic_bytes_per_launch": nbytes["route"]},
         "stages_ms": {"route": route_mean, "create_indices": statistics.fmean(index_ms),
+                      "route_index_fused": statistics.fmean(fused_ms),
                       "finalize": statistics.fmean(fin_stage_ms),
                       "route_plus_index_in_timed_steps": statistics.fmean(
                           [e[0].elapsed_time(e[1]) for e in ev]),
                       "step_median": statistics.median(step_ms),
-                      "note": "route/create_indices/finalize from a separate pass with an event "
-                              "between every stage; the timed steps carry events only at the "
-                              "step start, before finalize and at the step end"},
+                      "timed_steps_route_index": "fused" if fused else "separate",
+                      "note": "route/create_indices/finalize and route_index_fused from "
+                              "separate passes with an event between every stage; the timed "
+                              "steps carry events only at the step start, before finalize and "
+                              "at the step end"},
         "next_rows": {"permute": {
             "ms": perm_ms, "tokens_per_s": cfg.T / (perm_ms * 1e-3),
             "achieved_gbs": (2 * cfg.T * cfg.H + 2 * cfg.N * cfg.H + 4 * cfg.N) / (perm_ms * 1e-3) / 1e9,
@@ -488,6 +510,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "output_finite": out_ok,
+        "device_status_clean": status_ok,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

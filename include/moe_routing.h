@@ -5,7 +5,8 @@
  *
  * Sources (Mojo kernel library API pages, cited by page title and section):
  *   "group_limited_router_kernel"  -> moe_route
- *   "moe_create_indices"           -> moe_create_indices
+ *   "moe_create_indices"           -> moe_create_indices (fused with the
+ *                                     router: moe_route_index)
  *   "moe_finalize"                 -> moe_finalize
  *
  * Conventions for every entry point:
@@ -15,7 +16,7 @@
  *   - Every pointer is a DEVICE pointer to a dense row-major buffer owned by
  *     the caller. The library allocates nothing, frees nothing and keeps no
  *     state between calls; the index builder's scratch space is a
- *     caller-provided workspace.
+ *     caller-provided workspace (moe_route_index keeps a call counter there).
  *   - Every call only enqueues work on `stream` (0 = the legacy default
  *     stream) and returns without synchronising, except
  *     moe_read_device_status, which waits for the stream.
@@ -54,8 +55,10 @@ typedef enum {
   MOE_ERR_WORKSPACE = 6     /* workspace NULL or smaller than the size query returns */
 } moe_status_t;
 
-/* Bits of the device status word written by moe_create_indices. */
+/* Bits of the device status word written by moe_create_indices and moe_route_index. */
 #define MOE_DEVICE_STATUS_BAD_EXPERT_ID 0x1u /* some topk_ids entry was outside [0, E) */
+#define MOE_DEVICE_STATUS_SYNC_TIMEOUT 0x2u  /* moe_route_index: a cross-CTA wait gave up */
+#define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* moe_route_index: inconsistent exchanged counts */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024       /* n_routed_experts / n_experts */
@@ -176,6 +179,59 @@ moe_status_t moe_create_indices(uint32_t* token_expert_order, uint32_t* expert_s
                                 cudaStream_t stream);
 
 /*
+ * Workspace bytes that moe_route_index needs for num_tokens tokens and
+ * n_routed_experts experts (always >= 2048). Host-only; returns 0 for
+ * negative num_tokens or n_routed_experts outside [1, MOE_MAX_EXPERTS].
+ */
+size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_experts);
+
+/*
+ * moe_route_index -- moe_route_ex followed by moe_create_indices on its
+ * output, in one kernel launch.
+ * Pages "group_limited_router_kernel" (the routing: as moe_route and
+ * moe_route_ex) and "moe_create_indices" (the index: as moe_create_indices
+ * with topk_ids = expert_indices and num_slots = T*K). The pages launch the
+ * two as separate kernels; fusing them is this library's design.
+ *
+ * Every output is bit-identical to those of the two separate calls:
+ * expert_indices [T, K] int32 and expert_weights [T, K] fp32 (written, and
+ * also read back by the index build); token_expert_order [T*K],
+ * restore_token_order [T*K], expert_start_indices [E+1], expert_ids [E],
+ * expert_usage_stats [2] and the optional scales_offset_p [E+1] as described
+ * at moe_create_indices. Arguments and requirements are the union of
+ * moe_route_ex's and moe_create_indices', plus T*K < 2^32 - 1.
+ *
+ * workspace: device buffer of at least moe_route_index_workspace_size()
+ *   bytes, 256-byte aligned, caller-owned, ZERO-FILLED before its first use
+ *   (e.g. cudaMemset). Word 0 receives the device status word (read it with
+ *   moe_read_device_status); word 1 counts the calls made on the workspace;
+ *   the next 1024 bytes hold progress counters that each call zeroes for
+ *   the next one.
+ *   The CTAs of a call exchange their counts through words tagged with that
+ *   call's number, so nothing needs clearing between calls. Calls sharing one
+ *   workspace must not overlap.
+ * Execution: one cooperative launch (all CTAs resident at once; CTAs of up
+ *   to 1024 threads, at most one per 8 tokens). Every cross-CTA wait gives up
+ *   after one second; the call then sets MOE_DEVICE_STATUS_SYNC_TIMEOUT and
+ *   leaves the index outputs unspecified. MOE_DEVICE_STATUS_SYNC_STATE means
+ *   the exchanged counts were inconsistent, which only a workspace that was
+ *   not zero-filled can cause. After either bit, zero-fill the workspace
+ *   before the next call.
+ * Returns MOE_ERR_UNSUPPORTED when the kernel cannot be made resident (no
+ *   CTA fits on an SM), and MOE_ERR_CUDA when the cooperative launch fails.
+ */
+moe_status_t moe_route_index(int32_t* expert_indices, float* expert_weights,
+                             uint32_t* token_expert_order, uint32_t* expert_start_indices,
+                             uint32_t* restore_token_order, int32_t* expert_ids,
+                             uint32_t* expert_usage_stats, const float* expert_scores,
+                             const float* expert_bias, int64_t num_tokens,
+                             int32_t n_routed_experts, int32_t n_experts_per_tok,
+                             int32_t n_groups, int32_t topk_group, int32_t norm_weights,
+                             float routed_scaling_factor, moe_score_fn_t score_fn,
+                             void* workspace, size_t workspace_bytes, uint32_t* scales_offset_p,
+                             cudaStream_t stream);
+
+/*
  * moe_finalize -- fused unpermute gather + top-k weighted row sum.
  * Page "moe_finalize": description paragraph (gather each token's K rows of
  * down through restore_order, scale by the router weight, accumulate in
@@ -237,8 +293,8 @@ moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* input,
                          int32_t num_experts_per_token, int64_t hidden, cudaStream_t stream);
 
 /*
- * Reads the device status word that the last moe_create_indices call on
- * `workspace` wrote (0 = clean; MOE_DEVICE_STATUS_* bits otherwise). Enqueues
+ * Reads the device status word that the last moe_create_indices or
+ * moe_route_index call on `workspace` wrote (0 = clean; MOE_DEVICE_STATUS_* bits otherwise). Enqueues
  * a 4-byte copy on `stream` and waits for the stream to finish.
  */
 moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,

@@ -22,12 +22,14 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL_PTR", 2: "MOE_ERR_INVALID_ARG",
                 3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_UNSUPPORTED", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_WORKSPACE"}
 DEVICE_STATUS_BAD_EXPERT_ID = 0x1
+DEVICE_STATUS_SYNC_TIMEOUT = 0x2
+DEVICE_STATUS_SYNC_STATE = 0x4
 
 # Entry points declared in include/moe_routing.h.
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
                     "moe_create_indices", "moe_finalize", "moe_read_device_status",
                     "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex",
-                    "moe_route_ex")
+                    "moe_route_ex", "moe_route_index_workspace_size", "moe_route_index")
 
 
 class MoeError(RuntimeError):
@@ -73,6 +75,11 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, ctypes.c_int,
                                  vp]
     lib.moe_route_ex.restype = ctypes.c_int
+    lib.moe_route_index_workspace_size.argtypes = [i64, i32]
+    lib.moe_route_index_workspace_size.restype = sz
+    lib.moe_route_index.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
+                                    i32, f32, ctypes.c_int, vp, sz, vp, vp]
+    lib.moe_route_index.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -167,6 +174,43 @@ def moe_create_indices(token_expert_order: torch.Tensor, expert_start_indices: t
     rc = load_library().moe_create_indices(*args, N, E, ws, workspace.numel(), None,
                                            _stream(stream))
     _check("moe_create_indices", rc)
+
+
+def moe_route_index_workspace_size(num_tokens: int, n_routed_experts: int) -> int:
+    return int(load_library().moe_route_index_workspace_size(int(num_tokens),
+                                                             int(n_routed_experts)))
+
+
+def moe_route_index(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
+                    token_expert_order: torch.Tensor, expert_start_indices: torch.Tensor,
+                    restore_token_order: torch.Tensor, expert_ids: torch.Tensor,
+                    expert_usage_stats: torch.Tensor, expert_scores: torch.Tensor,
+                    expert_bias: torch.Tensor, n_groups: int, topk_group: int,
+                    norm_weights: bool, routed_scaling_factor: float, workspace: torch.Tensor,
+                    score_fn: int = SCORES_AS_GIVEN, scales_offset: torch.Tensor | None = None,
+                    stream=None) -> None:
+    """Router and index build in one launch; the workspace must be zero-filled
+    before its first use (each call leaves its counters at zero)."""
+    T, E = expert_scores.shape
+    K = expert_indices.shape[1] if expert_indices.dim() == 2 else 0
+    N = T * K
+    args = (_dev(expert_indices, "expert_indices", torch.int32, (T, K)),
+            _dev(expert_weights, "expert_weights", torch.float32, (T, K)),
+            _dev(token_expert_order, "token_expert_order", torch.int32, (N,)),
+            _dev(expert_start_indices, "expert_start_indices", torch.int32, (E + 1,)),
+            _dev(restore_token_order, "restore_token_order", torch.int32, (N,)),
+            _dev(expert_ids, "expert_ids", torch.int32, (E,)),
+            _dev(expert_usage_stats, "expert_usage_stats", torch.int32, (2,)),
+            _dev(expert_scores, "expert_scores", torch.float32),
+            _dev(expert_bias, "expert_bias", torch.float32, (E,)))
+    ws = _dev(workspace, "workspace", torch.uint8)
+    so = None if scales_offset is None else _dev(scales_offset, "scales_offset", torch.int32,
+                                                 (E + 1,))
+    rc = load_library().moe_route_index(*args, T, E, K, int(n_groups), int(topk_group),
+                                        int(bool(norm_weights)), float(routed_scaling_factor),
+                                        int(score_fn), ws, workspace.numel(), so,
+                                        _stream(stream))
+    _check("moe_route_index", rc)
 
 
 def moe_finalize(output: torch.Tensor, down: torch.Tensor, restore_order: torch.Tensor,
@@ -288,6 +332,49 @@ class IndexBuffers:
 
     def device_status(self, stream=None) -> int:
         return moe_read_device_status(self.workspace, stream)
+
+
+class RouteIndexBuffers:
+    """Preallocated outputs + zero-filled workspace of moe_route_index for T
+    tokens, E experts and K experts per token. The index outputs carry the
+    same names as IndexBuffers'."""
+
+    def __init__(self, T: int, E: int, K: int, device):
+        self.T, self.E, self.K, self.N = T, E, K, T * K
+        z = dict(dtype=torch.int32, device=device)
+        self.expert_indices = torch.empty((T, K), **z)
+        self.expert_weights = torch.empty((T, K), dtype=torch.float32, device=device)
+        self.token_expert_order = torch.empty(T * K, **z)
+        self.expert_start_indices = torch.empty(E + 1, **z)
+        self.restore_token_order = torch.empty(T * K, **z)
+        self.expert_ids = torch.empty(E, **z)
+        self.expert_usage_stats = torch.empty(2, **z)
+        ws = moe_route_index_workspace_size(T, E)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+
+    def run(self, expert_scores: torch.Tensor, expert_bias: torch.Tensor, n_groups: int,
+            topk_group: int, norm_weights: bool, routed_scaling_factor: float,
+            score_fn: int = SCORES_AS_GIVEN, scales_offset: torch.Tensor | None = None,
+            stream=None) -> "RouteIndexBuffers":
+        moe_route_index(self.expert_indices, self.expert_weights, self.token_expert_order,
+                        self.expert_start_indices, self.restore_token_order, self.expert_ids,
+                        self.expert_usage_stats, expert_scores, expert_bias, n_groups,
+                        topk_group, norm_weights, routed_scaling_factor, self.workspace,
+                        score_fn, scales_offset, stream)
+        return self
+
+    def device_status(self, stream=None) -> int:
+        return moe_read_device_status(self.workspace, stream)
+
+
+def route_index(expert_scores: torch.Tensor, expert_bias: torch.Tensor, n_experts_per_tok: int,
+                n_groups: int, topk_group: int, norm_weights: bool,
+                routed_scaling_factor: float, score_fn: int = SCORES_AS_GIVEN,
+                stream=None) -> RouteIndexBuffers:
+    T, E = expert_scores.shape
+    bufs = RouteIndexBuffers(T, E, n_experts_per_tok, expert_scores.device)
+    return bufs.run(expert_scores, expert_bias, n_groups, topk_group, norm_weights,
+                    routed_scaling_factor, score_fn, stream=stream)
 
 
 def create_indices(topk_ids: torch.Tensor, n_experts: int, stream=None) -> IndexBuffers:

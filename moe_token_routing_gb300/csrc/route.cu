@@ -17,421 +17,26 @@
 // Both read each score row once with coalesced (vector) loads, keep the bias
 // in registers across a persistent token loop, and write K ids and weights
 // per token.
-#include <math_constants.h>
-
-#include "common.cuh"
+#include "route_device.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;
-constexpr int kRouteWarps = kRouteThreads / 32;
-
-// With at most 32 groups and C experts per lane, a group always spans at
-// least one whole lane, so two layouts cover every shape.
-enum GroupMode : int {
-  kGroupsAllKept = 0,  // topk_group == n_groups: no group selection
-  kGroupsSegment = 1,  // a group spans a power-of-two run of whole lanes
-  kGroupsGeneric = 2   // anything else: group scores through shared memory
-};
-
-struct RouteArgs {
-  int32_t* ids;
-  float* weights;
-  const float* scores;
-  const float* bias;
-  int64_t T;
-  int E, K, G, M, S;
-  int norm;
-  float scale;
-  int group_mode;
-  int seg_lanes;  // lanes per group in kGroupsSegment
-  int score_fn;   // moe_score_fn_t applied to every loaded score
-};
-
-// exp(x) in fp32 by Cody-Waite range reduction (W. J. Cody and W. Waite,
-// "Software Manual for the Elementary Functions", 1980): x = n ln2 + r with
-// |r| <= ln2/2, ln2 split into a head with 12 trailing zero bits (so n*head is
-// exact) and a tail; exp(r) by its Taylor series to degree 7 in Horner form
-// with fused multiply-adds; 2^n assembled from exponent bits. x is clamped to
-// [-87, 88] so that 2^n is a normal float. Every step is a correctly rounded
-// fp32 operation, so the result is reproducible bit for bit.
-__device__ __forceinline__ float score_exp_f32(float x) {
-  x = fminf(fmaxf(x, -87.0f), 88.0f);
-  const float n = rintf(__fmul_rn(x, 1.44269504088896341f));
-  float r = __fmaf_rn(-n, 0.693145751953125f, x);
-  r = __fmaf_rn(-n, 1.42860682030941723e-6f, r);
-  float p = 1.98412698412698413e-4f;             // 1/7!
-  p = __fmaf_rn(p, r, 1.38888888888888889e-3f);  // 1/6!
-  p = __fmaf_rn(p, r, 8.33333333333333333e-3f);  // 1/5!
-  p = __fmaf_rn(p, r, 4.16666666666666667e-2f);  // 1/4!
-  p = __fmaf_rn(p, r, 1.66666666666666667e-1f);  // 1/3!
-  p = __fmaf_rn(p, r, 0.5f);
-  p = __fmaf_rn(p, r, 1.0f);
-  p = __fmaf_rn(p, r, 1.0f);
-  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
-}
-
-// The page's scores_input_fn: the score of (token, expert) from the loaded value.
-__device__ __forceinline__ float apply_score_fn(int fn, float x) {
-  if (fn == MOE_SCORES_SIGMOID) return __fdiv_rn(1.0f, __fadd_rn(1.0f, score_exp_f32(-x)));
-  return x;
-}
-
-// Running top-2 of a stream of values (multiset: equal values both count).
-__device__ __forceinline__ void top2_push(float& t1, float& t2, float x) {
-  t2 = fmaxf(t2, fminf(t1, x));
-  t1 = fmaxf(t1, x);
-}
-
-// Rank groups by (score desc, index asc) and return the bit mask of the M best.
-// Lane j < G holds g_j on entry.
-__device__ __forceinline__ uint32_t keep_best_groups(float gj, int lane, int G, int M) {
-  int ahead = 0;
-#pragma unroll 8
-  for (int j = 0; j < G; ++j) {
-    const float gx = __shfl_sync(kFullMask, gj, j);
-    ahead += (gx > gj) || (gx == gj && j < lane);
-  }
-  return __ballot_sync(kFullMask, lane < G && ahead < M);
-}
-
-// The C scores of row t that lane l owns (experts l*C .. l*C+C-1).
-template <int C, bool kVec>
-__device__ __forceinline__ void load_lane_scores(const RouteArgs& a, int64_t t, int e0,
-                                                 const bool (&valid)[C], float (&s)[C]) {
-  const float* row = a.scores + t * a.E;
-  if constexpr (kVec) {
-#pragma unroll
-    for (int q = 0; q < C / 4; ++q) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + 4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + e0 + 4 * q));
-      s[4 * q + 0] = v.x;
-      s[4 * q + 1] = v.y;
-      s[4 * q + 2] = v.z;
-      s[4 * q + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < C; ++c) s[c] = valid[c] ? __ldg(row + e0 + c) : 0.0f;
-  }
-}
-
-// Exact top-K by K rounds of a warp-wide max over each lane's best key; the
-// winning lane recomputes its best from all of its keys. Returns, in lane r <
-// K, the expert chosen in round r.
-template <int C>
-__device__ __forceinline__ int select_by_full_rounds(uint32_t (&key)[C], int lane, int e0, int K) {
-  uint32_t head = 0;
-  int head_pos = 0;
-#pragma unroll
-  for (int c = 0; c < C; ++c)
-    if (key[c] > head) { head = key[c]; head_pos = c; }
-  int my_id = 0;
-  for (int r = 0; r < K; ++r) {
-    const uint32_t best = __reduce_max_sync(kFullMask, head);
-    const unsigned holders = __ballot_sync(kFullMask, head == best && head != 0u);
-    const int win_lane = holders ? __ffs(holders) - 1 : 0;
-    const int id = __shfl_sync(kFullMask, e0 + head_pos, win_lane);
-    if (lane == r) my_id = id;
-    if (lane == win_lane) {
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        if (c == head_pos) key[c] = 0u;
-      head = 0;
-      head_pos = 0;
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        if (key[c] > head) { head = key[c]; head_pos = c; }
-    }
-  }
-  return my_id;
-}
-
 template <int C, bool kVec>
 __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kernel(const RouteArgs a) {
-  static_assert(C >= 2, "the warp path holds at least two experts per lane");
   extern __shared__ float dyn_smem[];  // kGroupsGeneric: kRouteWarps * E biased scores
   wait_for_prior_grid();
-
-  const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int e0 = lane * C;
-
-  float bias_r[C];
-  bool valid[C];
-  int n_valid = 0;
-#pragma unroll
-  for (int c = 0; c < C; ++c) {
-    const int e = e0 + c;
-    valid[c] = e < a.E;
-    bias_r[c] = valid[c] ? a.bias[e] : 0.0f;
-    n_valid += valid[c];
-  }
-  // In the segment layout a lane's experts all belong to one group.
-  const int lane_grp = n_valid > 0 ? e0 / a.S : 31;
-
-  const int64_t first = (int64_t)blockIdx.x * kRouteWarps + warp;
-  const int64_t stride = (int64_t)gridDim.x * kRouteWarps;
-  float s_next[C];
-  if (first < a.T) load_lane_scores<C, kVec>(a, first, e0, valid, s_next);
-
-  for (int64_t t = first; t < a.T; t += stride) {
-    float s[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) s[c] = s_next[c];
-    if (t + stride < a.T) load_lane_scores<C, kVec>(a, t + stride, e0, valid, s_next);
-    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
-#pragma unroll
-      for (int c = 0; c < C; ++c) s[c] = apply_score_fn(a.score_fn, s[c]);
-    }
-
-    float b[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) b[c] = valid[c] ? __fadd_rn(s[c], bias_r[c]) : -CUDART_INF_F;
-
-    int my_id = 0;
-    if (a.group_mode == kGroupsGeneric) {
-      // ---- groups through shared memory, then the exact full-round selection ----
-      float* wb = dyn_smem + warp * a.E;
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        if (valid[c]) wb[e0 + c] = b[c];
-      __syncwarp();
-      float gj = 0.0f;
-      if (lane < a.G) {
-        float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
-        for (int e = lane * a.S; e < (lane + 1) * a.S; ++e) top2_push(t1, t2, wb[e]);
-        gj = (a.S == 1) ? t1 : __fadd_rn(t1, t2);
-      }
-      __syncwarp();
-      const uint32_t kept = keep_best_groups(gj, lane, a.G, a.M);
-      uint32_t key[C];
-#pragma unroll
-      for (int c = 0; c < C; ++c)
-        key[c] = (valid[c] && ((kept >> ((e0 + c) / a.S)) & 1u)) ? ordered_key(b[c]) : 0u;
-      my_id = select_by_full_rounds<C>(key, lane, e0, a.K);
-    } else {
-      // ---- lane cache: the D best biased scores and their positions ----
-      // (ties keep the lower position, so equal entries come in expert order)
-      constexpr int D = C >= 3 ? 3 : 2;
-      float v[D];
-      int p[D];
-#pragma unroll
-      for (int j = 0; j < D; ++j) {
-        v[j] = 0.0f;
-        p[j] = 0;
-      }
-#pragma unroll
-      for (int c = 0; c < C; ++c) {
-        const float x = b[c];
-        bool g[D];
-#pragma unroll
-        for (int j = 0; j < D; ++j) g[j] = (j >= c) || x > v[j];  // empty slots take x
-#pragma unroll
-        for (int j = D - 1; j >= 1; --j) {
-          if (j > c) continue;
-          v[j] = g[j - 1] ? v[j - 1] : (g[j] ? x : v[j]);
-          p[j] = g[j - 1] ? p[j - 1] : (g[j] ? c : p[j]);
-        }
-        v[0] = g[0] ? x : v[0];
-        p[0] = g[0] ? c : p[0];
-      }
-
-      // ---- group selection (segment layout: the group's top-2 over its lanes) ----
-      bool lane_allowed = n_valid > 0;
-      if (a.group_mode == kGroupsSegment) {
-        float t1 = n_valid > 0 ? v[0] : -CUDART_INF_F, t2 = n_valid > 0 ? v[1] : -CUDART_INF_F;
-        for (int off = 1; off < a.seg_lanes; off <<= 1) {
-          const float o1 = __shfl_xor_sync(kFullMask, t1, off);
-          const float o2 = __shfl_xor_sync(kFullMask, t2, off);
-          t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
-          t1 = fmaxf(t1, o1);
-        }
-        const float g = __fadd_rn(t1, t2);
-        const float gj = __shfl_sync(kFullMask, g, lane < a.G ? lane * a.seg_lanes : 0);
-        const uint32_t kept = keep_best_groups(gj, lane, a.G, a.M);
-        lane_allowed = lane_allowed && ((kept >> lane_grp) & 1u);
-      }
-      const int n_allowed = lane_allowed ? n_valid : 0;
-
-      // ---- K rounds of a warp-wide max over the cached heads ----
-      uint32_t k[D];
-      int id[D];
-#pragma unroll
-      for (int j = 0; j < D; ++j) {
-        k[j] = n_allowed > j ? ordered_key(v[j]) : 0u;
-        id[j] = e0 + p[j];
-      }
-      int wins = 0;
-      uint32_t kth = 0;
-      int kth_id = 0;
-#pragma unroll 8
-      for (int r = 0; r < a.K; ++r) {
-        const uint32_t best = __reduce_max_sync(kFullMask, k[0]);
-        const unsigned holders = __ballot_sync(kFullMask, k[0] == best);
-        const int win_lane = __ffs(holders) - 1;
-        const int win_id = __shfl_sync(kFullMask, id[0], win_lane);
-        if (lane == r) my_id = win_id;
-        kth = best;
-        kth_id = win_id;
-        if (lane == win_lane) {
-#pragma unroll
-          for (int j = 0; j + 1 < D; ++j) {
-            k[j] = k[j + 1];
-            id[j] = id[j + 1];
-          }
-          k[D - 1] = 0u;
-          ++wins;
-        }
-      }
-
-      // ---- exactness check: a lane that gave up all D cached entries may hold
-      // a further candidate that should have won a later round ----
-      const bool needs_more = wins == D && n_allowed > D;
-      if (__any_sync(kFullMask, needs_more) || kth == 0u) {
-        float vn = -CUDART_INF_F;
-        int cn = -1;
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-          bool cached = false;
-#pragma unroll
-          for (int j = 0; j < D; ++j) cached = cached || c == p[j];
-          if (valid[c] && !cached && (cn < 0 || b[c] > vn)) { vn = b[c]; cn = c; }
-        }
-        const uint32_t kn = ordered_key(vn);
-        const bool beats = kn > kth || (kn == kth && e0 + cn < kth_id);
-        if (kth == 0u || __any_sync(kFullMask, needs_more && beats)) {
-          uint32_t key[C];
-#pragma unroll
-          for (int c = 0; c < C; ++c) key[c] = (valid[c] && lane_allowed) ? ordered_key(b[c]) : 0u;
-          my_id = select_by_full_rounds<C>(key, lane, e0, a.K);
-        }
-      }
-    }
-
-    // ---- weights: unbiased score, optional normalisation, scaling ----
-    const float* row = a.scores + t * a.E;
-    float w = (lane < a.K) ? apply_score_fn(a.score_fn, __ldg(row + my_id)) : 0.0f;
-    if (a.norm) {
-      float sum = 0.0f;
-#pragma unroll 8
-      for (int k = 0; k < a.K; ++k) sum = __fadd_rn(sum, __shfl_sync(kFullMask, w, k));
-      w = __fdiv_rn(w, sum);
-    }
-    w = __fmul_rn(w, a.scale);
-    if (lane < a.K) {
-      a.ids[t * a.K + lane] = my_id;
-      a.weights[t * a.K + lane] = w;
-    }
-  }
+  route_tokens_warp<C, kVec>(a, (int64_t)blockIdx.x * kRouteWarps + warp, a.T,
+                             (int64_t)gridDim.x * kRouteWarps, dyn_smem + warp * a.E,
+                             [](int64_t, int, int) {});
 }
 
-// One thread per token, E <= EP <= 32.
 template <int EP, bool kVec>
 __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const RouteArgs a) {
   wait_for_prior_grid();
-  float bias_r[EP];
-  uint32_t valid = 0, run_start = 0, run_end = 0;
-#pragma unroll
-  for (int e = 0; e < EP; ++e) {
-    const bool v = e < a.E;
-    bias_r[e] = v ? a.bias[e] : 0.0f;
-    valid |= (uint32_t)v << e;
-    if (v && e % a.S == 0) run_start |= 1u << e;
-    if (v && e % a.S == a.S - 1) run_end |= 1u << e;
-  }
-  const bool select_groups = a.M < a.G;
-
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < a.T; t += stride) {
-    const float* row = a.scores + t * a.E;
-    float s[EP];
-    if constexpr (kVec) {
-#pragma unroll
-      for (int q = 0; q < EP / 4; ++q) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * q < a.E) v = __ldg(reinterpret_cast<const float4*>(row + 4 * q));
-        s[4 * q + 0] = v.x;
-        s[4 * q + 1] = v.y;
-        s[4 * q + 2] = v.z;
-        s[4 * q + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EP; ++e) s[e] = ((valid >> e) & 1u) ? __ldg(row + e) : 0.0f;
-    }
-    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
-#pragma unroll
-      for (int e = 0; e < EP; ++e) s[e] = apply_score_fn(a.score_fn, s[e]);
-    }
-    float b[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) b[e] = __fadd_rn(s[e], bias_r[e]);
-
-    uint32_t allowed = valid;
-    if (select_groups) {
-      // g_end[e]: top-1 + top-2 of e's group so far; g_of[e]: the whole group's score
-      float g_end[EP], g_of[EP];
-      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if ((run_start >> e) & 1u) t1 = t2 = -CUDART_INF_F;
-        top2_push(t1, t2, b[e]);
-        g_end[e] = (a.S == 1) ? t1 : __fadd_rn(t1, t2);
-      }
-      g_of[EP - 1] = g_end[EP - 1];
-#pragma unroll
-      for (int e = EP - 2; e >= 0; --e) g_of[e] = ((run_end >> e) & 1u) ? g_end[e] : g_of[e + 1];
-      // rank each group leader against the other leaders
-      uint32_t kept_leaders = 0;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (!((run_start >> e) & 1u)) continue;
-        int ahead = 0;
-#pragma unroll
-        for (int f = 0; f < EP; ++f) {
-          if (!((run_start >> f) & 1u)) continue;
-          ahead += (g_of[f] > g_of[e]) || (g_of[f] == g_of[e] && f < e);
-        }
-        if (ahead < a.M) kept_leaders |= 1u << e;
-      }
-      allowed = 0;
-      bool keep = false;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if ((run_start >> e) & 1u) keep = (kept_leaders >> e) & 1u;
-        if (keep && ((valid >> e) & 1u)) allowed |= 1u << e;
-      }
-    }
-
-    uint32_t key[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) key[e] = ((allowed >> e) & 1u) ? ordered_key(b[e]) : 0u;
-
-    float sum = 0.0f;
-    int32_t* ids_row = a.ids + t * a.K;
-    float* w_row = a.weights + t * a.K;
-    for (int r = 0; r < a.K; ++r) {
-      uint32_t best = 0;
-      int best_e = 0;
-      float best_s = 0.0f;
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (key[e] > best) { best = key[e]; best_e = e; best_s = s[e]; }
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e == best_e) key[e] = 0u;
-      ids_row[r] = best_e;
-      w_row[r] = best_s;
-      sum = __fadd_rn(sum, best_s);
-    }
-    for (int r = 0; r < a.K; ++r) {
-      float w = w_row[r];
-      if (a.norm) w = __fdiv_rn(w, sum);
-      w_row[r] = __fmul_rn(w, a.scale);
-    }
-  }
+  route_tokens_thread<EP, kVec>(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, a.T,
+                                (int64_t)gridDim.x * blockDim.x, [](int64_t, int, int) {});
 }
 
 template <typename Kernel>
@@ -458,87 +63,43 @@ moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, 
 }
 
 template <int C>
-moe_status_t launch_warp_path(const RouteArgs& a, bool vec, cudaStream_t stream) {
-  const size_t smem =
-      a.group_mode == kGroupsGeneric ? (size_t)kRouteWarps * a.E * sizeof(float) : 0;
+moe_status_t launch_warp_path(const RoutePlan& p, cudaStream_t stream) {
+  const size_t smem = route_group_smem(p);
   if constexpr (C % 4 == 0) {
-    if (vec) return launch_route(route_warp_kernel<C, true>, a, kRouteWarps, smem, stream);
+    if (p.vec) return launch_route(route_warp_kernel<C, true>, p.a, kRouteWarps, smem, stream);
   }
-  return launch_route(route_warp_kernel<C, false>, a, kRouteWarps, smem, stream);
+  return launch_route(route_warp_kernel<C, false>, p.a, kRouteWarps, smem, stream);
 }
 
 template <int EP>
-moe_status_t launch_thread_path(const RouteArgs& a, bool vec, cudaStream_t stream) {
-  if (vec) return launch_route(route_thread_kernel<EP, true>, a, kRouteThreads, 0, stream);
-  return launch_route(route_thread_kernel<EP, false>, a, kRouteThreads, 0, stream);
+moe_status_t launch_thread_path(const RoutePlan& p, cudaStream_t stream) {
+  if (p.vec) return launch_route(route_thread_kernel<EP, true>, p.a, kRouteThreads, 0, stream);
+  return launch_route(route_thread_kernel<EP, false>, p.a, kRouteThreads, 0, stream);
 }
-
-bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-
-}  // namespace
-}  // namespace moe
-
-namespace moe {
-namespace {
 
 moe_status_t route_impl(int32_t* expert_indices, float* expert_weights,
                         const float* expert_scores, const float* expert_bias, int64_t num_tokens,
                         int32_t n_routed_experts, int32_t n_experts_per_tok, int32_t n_groups,
                         int32_t topk_group, int32_t norm_weights, float routed_scaling_factor,
                         int32_t score_fn, cudaStream_t stream) {
-  const int E = n_routed_experts, K = n_experts_per_tok, G = n_groups, M = topk_group;
-  if (num_tokens < 0 || E < 1 || G < 1 || M < 1 || K < 1) return MOE_ERR_INVALID_ARG;
-  if (E % G != 0 || M > G) return MOE_ERR_INVALID_ARG;
-  const int S = E / G;
-  if ((int64_t)K > (int64_t)M * S) return MOE_ERR_INVALID_ARG;
-  if (E > MOE_MAX_EXPERTS || G > MOE_MAX_GROUPS || K > MOE_MAX_EXPERTS_PER_TOK)
-    return MOE_ERR_UNSUPPORTED;
-  if (num_tokens > (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
+  RoutePlan p;
+  moe_status_t st = plan_route(expert_indices, expert_weights, expert_scores, expert_bias,
+                               num_tokens, n_routed_experts, n_experts_per_tok, n_groups,
+                               topk_group, norm_weights, routed_scaling_factor, score_fn, &p);
+  if (st != MOE_OK) return st;
   if (num_tokens == 0) return MOE_OK;
-  if (!expert_indices || !expert_weights || !expert_scores || !expert_bias)
-    return MOE_ERR_NULL_PTR;
-  if (!aligned(expert_indices, 4) || !aligned(expert_weights, 4) || !aligned(expert_scores, 4) ||
-      !aligned(expert_bias, 4))
-    return MOE_ERR_MISALIGNED;
-
-  RouteArgs a;
-  a.ids = expert_indices;
-  a.weights = expert_weights;
-  a.scores = expert_scores;
-  a.bias = expert_bias;
-  a.T = num_tokens;
-  a.E = E;
-  a.K = K;
-  a.G = G;
-  a.M = M;
-  a.S = S;
-  a.norm = norm_weights != 0;
-  a.scale = routed_scaling_factor;
-  a.group_mode = kGroupsAllKept;
-  a.seg_lanes = 1;
-  a.score_fn = score_fn;
-  const bool vec = (E % 4 == 0) && aligned(expert_scores, 16);
-
-  if (E <= 32) {
-    if (E <= 8) return launch_thread_path<8>(a, vec, stream);
-    if (E <= 16) return launch_thread_path<16>(a, vec, stream);
-    return launch_thread_path<32>(a, vec, stream);
-  }
-  const int C = E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
-  if (M < G) {
-    if (S % C == 0 && is_pow2(S / C)) {
-      a.group_mode = kGroupsSegment;
-      a.seg_lanes = S / C;
-    } else {
-      a.group_mode = kGroupsGeneric;
-    }
-  }
-  switch (C) {
-    case 2: return launch_warp_path<2>(a, vec, stream);
-    case 4: return launch_warp_path<4>(a, vec, stream);
-    case 8: return launch_warp_path<8>(a, vec, stream);
-    case 16: return launch_warp_path<16>(a, vec, stream);
-    default: return launch_warp_path<32>(a, vec, stream);
+  st = check_route_pointers(p.a);
+  if (st != MOE_OK) return st;
+  switch (p.C) {
+    case 0:
+      if (p.EP == 8) return launch_thread_path<8>(p, stream);
+      if (p.EP == 16) return launch_thread_path<16>(p, stream);
+      return launch_thread_path<32>(p, stream);
+    case 2: return launch_warp_path<2>(p, stream);
+    case 4: return launch_warp_path<4>(p, stream);
+    case 8: return launch_warp_path<8>(p, stream);
+    case 16: return launch_warp_path<16>(p, stream);
+    default: return launch_warp_path<32>(p, stream);
   }
 }
 
@@ -563,8 +124,6 @@ extern "C" moe_status_t moe_route_ex(int32_t* expert_indices, float* expert_weig
                                      int32_t topk_group, int32_t norm_weights,
                                      float routed_scaling_factor, moe_score_fn_t score_fn,
                                      cudaStream_t stream) {
-  if (score_fn != MOE_SCORES_AS_GIVEN && score_fn != MOE_SCORES_SIGMOID)
-    return MOE_ERR_UNSUPPORTED;
   return moe::route_impl(expert_indices, expert_weights, expert_scores, expert_bias, num_tokens,
                          n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights,
                          routed_scaling_factor, score_fn, stream);

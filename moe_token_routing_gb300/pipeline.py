@@ -14,19 +14,30 @@ from __future__ import annotations
 
 import torch
 
-from .binding import IndexBuffers, moe_finalize, moe_permute, moe_route
+from .binding import (IndexBuffers, moe_finalize, moe_permute, moe_read_device_status,
+                      moe_route, moe_route_index,
+                      moe_route_index_workspace_size)
 
 
 class RoutingPipeline:
+    """``fused=True`` runs route and create_indices as one launch
+    (moe_route_index); the outputs are the same bits either way."""
+
     def __init__(self, T: int, E: int, K: int, H: int, n_groups: int, topk_group: int,
-                 norm_weights: bool, routed_scaling_factor: float, device="cuda"):
+                 norm_weights: bool, routed_scaling_factor: float, device="cuda",
+                 fused: bool = False):
         self.T, self.E, self.K, self.H = T, E, K, H
         self.n_groups, self.topk_group = n_groups, topk_group
         self.norm_weights, self.scale = bool(norm_weights), float(routed_scaling_factor)
         self.device = torch.device(device)
+        self.fused = bool(fused)
         self.expert_indices = torch.empty((T, K), dtype=torch.int32, device=self.device)
         self.expert_weights = torch.empty((T, K), dtype=torch.float32, device=self.device)
         self.index = IndexBuffers(T * K, E, self.device)
+        self.fused_workspace = None
+        if self.fused:
+            self.fused_workspace = torch.zeros(moe_route_index_workspace_size(T, E),
+                                               dtype=torch.uint8, device=self.device)
         self.output = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
         self._staged = None
 
@@ -36,6 +47,29 @@ class RoutingPipeline:
 
     def create_indices(self, stream=None):
         self.index.run(self.expert_indices, stream)
+
+    def route_index(self, expert_scores, expert_bias, stream=None):
+        """route + create_indices in one launch (needs ``fused=True``)."""
+        if self.fused_workspace is None:
+            raise RuntimeError("RoutingPipeline was built with fused=False")
+        ix = self.index
+        moe_route_index(self.expert_indices, self.expert_weights, ix.token_expert_order,
+                        ix.expert_start_indices, ix.restore_token_order, ix.expert_ids,
+                        ix.expert_usage_stats, expert_scores, expert_bias, self.n_groups,
+                        self.topk_group, self.norm_weights, self.scale, self.fused_workspace,
+                        stream=stream)
+
+    def route_and_index(self, expert_scores, expert_bias, stream=None):
+        if self.fused:
+            self.route_index(expert_scores, expert_bias, stream)
+        else:
+            self.route(expert_scores, expert_bias, stream)
+            self.create_indices(stream)
+
+    def device_status(self, stream=None) -> int:
+        """Device status word of the last index build (0 = clean)."""
+        ws = self.fused_workspace if self.fused else self.index.workspace
+        return moe_read_device_status(ws, stream)
 
     def finalize(self, down, stream=None, output=None):
         moe_finalize(self.output if output is None else output, down,
@@ -47,8 +81,7 @@ class RoutingPipeline:
         return out
 
     def __call__(self, expert_scores, expert_bias, down, stream=None) -> torch.Tensor:
-        self.route(expert_scores, expert_bias, stream)
-        self.create_indices(stream)
+        self.route_and_index(expert_scores, expert_bias, stream)
         self.finalize(down, stream)
         return self.output
 
@@ -130,8 +163,7 @@ class HostStreamer:
             slot["down"].copy_(down_h, non_blocking=True)
             slot["copied_in"].record(self.copy_in)
         self.compute.wait_event(slot["copied_in"])
-        self.pipe.route(slot["scores"], slot["bias"], self.compute)
-        self.pipe.create_indices(self.compute)
+        self.pipe.route_and_index(slot["scores"], slot["bias"], self.compute)
         self.pipe.finalize(slot["down"], self.compute, output=slot["out"])
         slot["computed"].record(self.compute)
         self.copy_out.wait_event(slot["computed"])

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
          "moe_create_indices", "moe_finalize", "moe_read_device_status",
-         "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex", "moe_route_ex"])
+         "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex", "moe_route_ex",
+         "moe_route_index_workspace_size", "moe_route_index"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -55,6 +56,28 @@ def test_workspace_size_query(lib):
     assert lib.moe_create_indices_workspace_size(-1, 8) == 0
     assert lib.moe_create_indices_workspace_size(10, 0) == 0
     assert lib.moe_create_indices_workspace_size(10, 1025) == 0
+
+
+def route_index_workspace_bytes(T, E):
+    """256-byte header, four 256-byte counter blocks, then [E][R] tagged counts
+    and prefixes, E tagged totals
+    and R tagged status words (8 bytes each), every part rounded up to 256
+    bytes; R = the CTA bound (one CTA per 8 tokens, at most 2048) rounded up to 4."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    ctas = min(max((T + 7) // 8, 1), 2048)
+    R = (ctas + 3) // 4 * 4
+    return 256 + 1024 + 2 * r256(8 * E * R) + r256(8 * E) + r256(8 * R)
+
+
+def test_route_index_workspace_size_query(lib):
+    f = lib.moe_route_index_workspace_size
+    for T, E in ((0, 8), (64, 256), (16384, 256), (131072, 8), (10 ** 9, 1024), (33, 96)):
+        assert f(T, E) == route_index_workspace_bytes(T, E), (T, E)
+    assert f(0, 8) == 2304
+    assert f(16384, 256) == 256 + 1024 + 2 * 8 * 256 * 2048 + 2048 + 8 * 2048
+    assert f(-1, 8) == 0
+    assert f(10, 0) == 0
+    assert f(10, 1025) == 0
 
 
 FAKE = 0x7f0000001000  # never dereferenced: every call below fails host validation
@@ -97,6 +120,27 @@ def test_create_indices_host_validation(lib):
     assert f(*outs, 10, 2000, FAKE, ws, None, None) == 4
     assert f(FAKE, None, FAKE, FAKE, FAKE, FAKE, 10, 64, FAKE, ws, None, None) == 1
     assert f(FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE, 10, 64, FAKE, ws, None, None) == 3
+
+
+def test_route_index_host_validation(lib):
+    f = lib.moe_route_index
+    outs = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    ins = (FAKE, FAKE)
+    ws = lib.moe_route_index_workspace_size(1000, 256)
+    cfg = (1000, 256, 8, 8, 4, 1, 1.0)
+    assert f(*outs, *ins, *cfg, 7, FAKE, ws, None, None) == 4          # unknown score loader
+    assert f(*outs, *ins, 1000, 256, 8, 7, 4, 1, 1.0, 0, FAKE, ws, None, None) == 2  # E % G
+    assert f(*outs, *ins, 1000, 256, 0, 8, 4, 1, 1.0, 0, FAKE, ws, None, None) == 2  # K < 1
+    big = 0x80000000  # T * K = 2^32 slots: beyond the uint32 index outputs
+    assert f(*outs, *ins, big, 256, 2, 8, 4, 1, 1.0, 0, FAKE, ws, None, None) == 4
+    assert f(*outs, *ins, *cfg, 0, FAKE, ws - 1, None, None) == 6      # workspace too small
+    assert f(*outs, *ins, *cfg, 0, None, ws, None, None) == 6          # no workspace
+    assert f(*outs, *ins, *cfg, 0, FAKE + 64, ws, None, None) == 3     # workspace alignment
+    assert f(FAKE, FAKE, None, *outs[3:], *ins, *cfg, 0, FAKE, ws, None, None) == 1
+    assert f(*outs[:3], None, *outs[4:], *ins, *cfg, 0, FAKE, ws, None, None) == 1
+    assert f(*outs, None, FAKE, *cfg, 0, FAKE, ws, None, None) == 1    # no scores
+    assert f(*outs[:2], FAKE + 2, *outs[3:], *ins, *cfg, 0, FAKE, ws, None, None) == 3
+    assert f(*outs, *ins, *cfg, 0, FAKE, ws, FAKE + 1, None) == 3      # scales_offset alignment
 
 
 def test_finalize_host_validation(lib):

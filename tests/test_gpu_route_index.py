@@ -1,0 +1,251 @@
+"""GPU parity of moe_route_index: the group-limited router (page
+"group_limited_router_kernel") and the index build (page "moe_create_indices")
+in one cooperative launch, against the oracle's route followed by its
+create_indices.
+
+Ids and every index output are bit-exact; the weights are the router's fp32
+arithmetic and are compared bit for bit as well (the same device code makes
+them). The bounded wait of the cross-CTA hand-off is driven by a small
+harness (tests/cuda) on a word that nothing tags: it must give up within its
+one-second bound and leave the GPU usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _workloads import workload
+
+pytestmark = pytest.mark.gpu
+
+INDEX_KEYS = ("token_expert_order", "expert_start_indices", "restore_token_order", "expert_ids",
+              "expert_usage_stats")
+
+
+def _moe():
+    import moe_token_routing_gb300 as moe
+    moe.load_library()
+    return moe
+
+
+def gpu_route_index(scores, bias, K, G, M, norm, scale, score_fn=0, scales=False, bufs=None):
+    moe = _moe()
+    s = torch.from_numpy(np.ascontiguousarray(scores)).cuda()
+    b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
+    T, E = scores.shape
+    if bufs is None:
+        bufs = moe.RouteIndexBuffers(T, E, K, "cuda")
+    so = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda") if scales else None
+    bufs.run(s, b, G, M, norm, scale, score_fn, scales_offset=so)
+    torch.cuda.synchronize()
+    out = {k: getattr(bufs, k).cpu().numpy() for k in INDEX_KEYS}
+    for k in INDEX_KEYS:
+        if k != "expert_ids":
+            out[k] = out[k].view(np.uint32)
+    out["ids"] = bufs.expert_indices.cpu().numpy()
+    out["weights"] = bufs.expert_weights.cpu().numpy()
+    if scales:
+        out["scales"] = so.cpu().numpy().view(np.uint32)
+    return out, bufs
+
+
+def assert_parity(got, ids_ref, w_ref, idx_ref, E):
+    bad = np.nonzero((got["ids"] != ids_ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} token rows differ, first {bad[:1]}"
+    assert np.array_equal(got["weights"].view(np.uint32), w_ref.view(np.uint32))
+    for k in INDEX_KEYS:
+        assert np.array_equal(got[k], idx_ref[k]), k
+
+
+def check(scores, bias, K, G, M, norm, scale, **kw):
+    ids_ref, w_ref = oracle.route(scores, bias, K, G, M, norm, scale)
+    idx_ref = oracle.create_indices(ids_ref, scores.shape[1])
+    got, bufs = gpu_route_index(scores, bias, K, G, M, norm, scale, **kw)
+    assert_parity(got, ids_ref, w_ref, idx_ref, scores.shape[1])
+    assert bufs.device_status() == 0
+    return got, bufs, ids_ref
+
+
+@pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
+def test_parity_on_workloads(name):
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+    assert bufs.device_status() == 0
+
+
+# (E, G, M, K): thread path (E <= 32), warp path with every group layout
+# (all kept, power-of-two lane segments, shared-memory groups), and C = 2 .. 32.
+SHAPES = [(8, 1, 1, 2), (8, 4, 2, 3), (12, 3, 2, 4), (16, 4, 2, 4), (32, 4, 2, 8),
+          (48, 4, 2, 6), (64, 8, 4, 8), (96, 4, 2, 8), (120, 5, 2, 8), (128, 1, 1, 8),
+          (160, 8, 3, 6), (256, 8, 4, 8), (256, 1, 1, 32), (384, 12, 4, 8), (512, 8, 2, 16),
+          (1024, 32, 4, 8)]
+
+
+@pytest.mark.parametrize("E,G,M,K", SHAPES)
+@pytest.mark.parametrize("T", [1, 333, 5000])
+def test_parity_shapes(E, G, M, K, T):
+    rng = np.random.default_rng(E * 7919 + G * 31 + M * 7 + K + T)
+    scores = rng.random((T, E), dtype=np.float32)
+    bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    check(scores, bias, K, G, M, True, 1.5)
+
+
+@pytest.mark.parametrize("T", [0, 1, 7, 8, 9, 255, 257, 4097, 100003])
+def test_token_counts_prefill_shape(T):
+    cfg = synth.get_config("dsv3_prefill")
+    scores = synth.make_scores(cfg, n_tokens=T) if T else np.zeros((0, cfg.E), np.float32)
+    bias = synth.make_bias(cfg)
+    got, _, _ = check(scores, bias, cfg.K, cfg.G, cfg.M, True, 2.5)
+    if T == 0:
+        assert (got["expert_ids"] == -1).all() and (got["expert_start_indices"] == 0).all()
+        assert got["expert_usage_stats"].tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("E,G,M,K,T", [(8, 1, 1, 2, 2_000_000), (64, 8, 4, 8, 200_000)])
+def test_several_placement_rounds_per_cta(E, G, M, K, T):
+    """More than 2048 slots per CTA, so each CTA places its slots in several
+    rounds (thread path and warp path)."""
+    rng = np.random.default_rng(T)
+    scores = rng.random((T, E), dtype=np.float32)
+    bias = np.zeros(E, np.float32)
+    check(scores, bias, K, G, M, False, 1.0)
+
+
+def test_hot_experts_and_ties():
+    """Scores on a 1/8 grid plus a large bias on four experts: many equal keys
+    and a few experts holding most slots."""
+    rng = np.random.default_rng(5)
+    T, E = 20000, 128
+    scores = (rng.integers(0, 9, size=(T, E)) / 8).astype(np.float32)
+    bias = np.zeros(E, np.float32)
+    bias[[3, 17, 64, 100]] = 2.0
+    got, _, _ = check(scores, bias, 8, 8, 4, True, 1.0)
+    assert got["expert_usage_stats"][0] >= T // 2
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_prefill", "few_expert_large_batch"])
+def test_sigmoid_loader(name):
+    cfg = synth.get_config(name)
+    logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
+    bias = synth.make_bias(cfg)
+    ids_ref, w_ref = oracle.route(oracle.sigmoid(logits), bias, cfg.K, cfg.G, cfg.M,
+                                  cfg.norm_weights, cfg.scale)
+    idx_ref = oracle.create_indices(ids_ref, cfg.E)
+    moe = _moe()
+    got, _ = gpu_route_index(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                             score_fn=moe.SCORES_SIGMOID)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3_prefill", "skewed_ungrouped"])
+def test_scales_offsets(name):
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
+    got, _ = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                             scales=True)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+    assert np.array_equal(got["scales"], oracle.scales_offsets(ids_ref, cfg.E))
+
+
+def test_call_counter_advances_and_calls_repeat():
+    """Header word 1 counts the calls; nothing is cleared between calls."""
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("dsv3_prefill")
+    bufs = None
+    for n in range(1, 4):
+        got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
+                                    cfg.scale, bufs=bufs)
+        assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+        header = bufs.workspace[:8].view(torch.int32).cpu().numpy()
+        assert header.tolist() == [0, n]
+
+
+def test_workspace_reused_across_shapes():
+    """Words left tagged by a larger call never pass for a smaller call's."""
+    moe = _moe()
+    big = synth.get_config("dsv3_prefill")
+    ws = torch.zeros(moe.moe_route_index_workspace_size(big.T, big.E), dtype=torch.uint8,
+                     device="cuda")
+    for name in ("dsv3_prefill", "dsv3_decode", "tiny", "dsv3_prefill"):
+        cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
+        bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda")
+        bufs.workspace = ws
+        got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
+                                    cfg.scale, bufs=bufs)
+        assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+        assert bufs.device_status() == 0
+
+
+def test_call_counter_wraps_past_zero():
+    """Call number 0 is skipped, so a zero-filled word never looks current."""
+    moe = _moe()
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("skewed_ungrouped")
+    bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda")
+    bufs.workspace[:8].view(torch.int32)[1] = -1
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                                bufs=bufs)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+    assert bufs.device_status() == 0
+    assert bufs.workspace[:8].view(torch.int32)[1].item() == 1
+
+
+def _selftest_lib():
+    """The bounded-wait harness of tests/cuda, built with nvcc for sm_103a."""
+    import ctypes
+    import os
+    import subprocess
+    from moe_token_routing_gb300 import build
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "cuda", "tagged_sync_selftest.cu")
+    so = os.path.join(here, "cuda", "libtagged_sync_selftest.so")
+    hdr = os.path.join(os.path.dirname(os.path.abspath(build.__file__)), "csrc")
+    if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+        subprocess.run([build.nvcc()] + build.ARCH_FLAGS + ["-O2", "-std=c++17", "-Xcompiler",
+                        "-fPIC", "-shared", "-I", hdr, "-I", os.path.join(build.ROOT, "include"),
+                        src, "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    vp = ctypes.c_void_p
+    lib.tagged_sync_selftest.argtypes = [vp, ctypes.c_uint32, ctypes.c_int, vp, vp]
+    lib.tagged_sync_selftest.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("publish", [True, False])
+def test_bounded_wait(publish):
+    """The wait of the cross-CTA hand-off: with a producer it returns the
+    value; with none (a word that nothing tags) it gives up after its one
+    second limit and reports failure, and the GPU stays usable."""
+    lib = _selftest_lib()
+    word = torch.zeros(1, dtype=torch.int64, device="cuda")
+    out = torch.full((2,), 7, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = lib.tagged_sync_selftest(word.data_ptr(), 5, int(publish), out.data_ptr(),
+                                  elapsed.data_ptr())
+    assert rc == 0
+    ok, value = out.cpu().tolist()
+    seconds = elapsed.item() * 1e-9
+    if publish:
+        assert ok == 1 and value == 1234 and seconds < 0.5
+    else:
+        assert ok == 0 and 0.9 < seconds < 5.0
+    # the context is still healthy
+    assert torch.ones(4, device="cuda").sum().item() == 4.0
+
+
+def test_fused_pipeline_matches_separate_launches():
+    moe = _moe()
+    cfg, scores, bias, *_ = workload("skewed_ungrouped")
+    s = torch.from_numpy(scores).cuda()
+    b = torch.from_numpy(bias).cuda()
+    down = torch.from_numpy(synth.make_down(cfg).view(np.int16)).cuda().view(torch.bfloat16)
+    outs = []
+    for fused in (False, True):
+        pipe = moe.RoutingPipeline(cfg.T, cfg.E, cfg.K, cfg.H, cfg.G, cfg.M, cfg.norm_weights,
+                                   cfg.scale, fused=fused)
+        out = pipe(s, b, down).clone()
+        torch.cuda.synchronize()
+        assert pipe.device_status() == 0
+        outs.append((out, pipe.index.restore_token_order.clone(), pipe.expert_weights.clone()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
