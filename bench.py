@@ -65,9 +65,9 @@ def dist_env():
 
 def index_launches(num_slots: int, n_experts: int) -> int:
     """Kernels one moe_create_indices call launches: one CTA does everything for
-    N <= 2048 slots; otherwise count + scatter, plus a scan kernel when the
-    count matrix (experts x 2048-slot chunks, rows padded to 4) exceeds 32Ki words."""
-    chunks = -(-num_slots // 2048)
+    N <= 1024 slots; otherwise count + scatter, plus a scan kernel when the
+    count matrix (experts x 1024-slot chunks, rows padded to 4) exceeds 32Ki words."""
+    chunks = -(-num_slots // 1024)
     if chunks <= 1:
         return 1
     row = (chunks + 3) // 4 * 4

@@ -9,19 +9,19 @@
 // here positions are computed arithmetically, so any count per expert works.
 //
 // Design (no inter-CTA waits, deterministic, stable):
-//   count   : CTA b counts the experts of its 2048 slots (warp-aggregated with
+//   count   : CTA b counts the experts of its 1024 slots (warp-aggregated with
 //             match.any, shared-memory counters) -> counts[e][b] (expert-major,
 //             so one expert's counts are contiguous).
 //   scatter : CTA b derives its bases itself from the small count matrix:
 //             base[b][e] = start(e) + sum_{b' < b} counts[e][b'], with start(e)
 //             the exclusive sum of the per-expert totals; CTA 0 also writes the
 //             compact CSR, expert_ids, usage stats and the device status word.
-//             Then it re-reads its slots; within a CTA each warp owns 256
+//             Then it re-reads its slots; within a CTA each warp owns 128
 //             consecutive slots, so a slot's position is base[b][e] + (slots of
 //             e in earlier warps) + (slots of e in earlier steps of its warp) +
 //             (lower lanes of its step with the same e). Writes
 //             token_expert_order and restore_token_order in one pass.
-//   For N <= 2048 one CTA does everything in one launch. When the count matrix
+//   For N <= 1024 one CTA does everything in one launch. When the count matrix
 //   is too large for every CTA to read it (more than 32Ki words), a one-CTA
 //   scan kernel turns the counts into bases in between.
 #include <mutex>
@@ -203,7 +203,11 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     }
     if (threadIdx.x == 0) s_flags = 0;
     __syncthreads();
-    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp, b == 0);  // s_base[e] := start(e)
+    // s_base[e] := start(e); only CTA 0 needs the rest of the expert table
+    if (b == 0)
+      emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
+    else
+      block_exclusive_scan(s_base, a.E, warp_tmp);
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
     if (b == 0) {
       uint32_t f = 0;

@@ -11,9 +11,9 @@ namespace {
 
 constexpr int kIdxThreads = 256;
 constexpr int kIdxWarps = kIdxThreads / 32;
-constexpr int kStepsPerWarp = 8;
+constexpr int kStepsPerWarp = 4;
 constexpr int kSlotsPerWarp = 32 * kStepsPerWarp;
-constexpr int kSlotsPerCta = kIdxWarps * kSlotsPerWarp;  // 2048
+constexpr int kSlotsPerCta = kIdxWarps * kSlotsPerWarp;  // 1024
 constexpr int kScanThreads = 1024;
 constexpr uint32_t kScaleRowAlign = MOE_SCALES_ROW_ALIGNMENT;
 

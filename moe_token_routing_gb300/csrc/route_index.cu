@@ -174,8 +174,8 @@ __device__ bool scan_row(const FusedArgs& f, int e, uint32_t tag) {
 // slot of expert e goes to s_base[e] (the CTA's first position for e) +
 // warp_off[e] (slots of e before it in this CTA, advanced per step) + the
 // lower lanes of its step with the same e.
-// Loads the ids of the 256 slots c0 .. c0+255 (below s1) that the calling
-// warp places in one round: -1 marks a slot past s1 or an id outside [0, E).
+// Loads the ids of the 32 * kStepsPerWarp slots from c0 on (below s1) that
+// the calling warp places in one round: -1 marks a slot past s1 or an id outside [0, E).
 __device__ __forceinline__ void load_round(const FusedArgs& f, int64_t c0, int64_t s1,
                                            int (&v)[kStepsPerWarp], bool& bad) {
   const int lane = threadIdx.x & 31, E = f.x.E;

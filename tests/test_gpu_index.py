@@ -47,7 +47,7 @@ def test_parity_on_workloads(name):
         assert np.array_equal(got[k], ref[k]), k
 
 
-@pytest.mark.parametrize("N", [0, 1, 31, 2047, 2048, 2049, 4113, 100003])
+@pytest.mark.parametrize("N", [0, 1, 31, 1023, 1024, 1025, 2047, 2048, 2049, 4113, 100003])
 @pytest.mark.parametrize("E", [1, 3, 8, 64, 256, 1000, 1024])
 def test_random_ids(N, E):
     rng = np.random.default_rng(N * 31 + E)

@@ -105,8 +105,8 @@ def test_token_counts_prefill_shape(T):
 
 @pytest.mark.parametrize("E,G,M,K,T", [(8, 1, 1, 2, 2_000_000), (64, 8, 4, 8, 200_000)])
 def test_several_placement_rounds_per_cta(E, G, M, K, T):
-    """More than 2048 slots per CTA, so each CTA places its slots in several
-    rounds (thread path and warp path)."""
+    """Many more slots per warp than one placement round holds, so each warp
+    places its slots in several rounds (thread path and warp path)."""
     rng = np.random.default_rng(T)
     scores = rng.random((T, E), dtype=np.float32)
     bias = np.zeros(E, np.float32)
