@@ -65,13 +65,8 @@ def dist_env():
 
 def index_launches(num_slots: int, n_experts: int) -> int:
     """Kernels one moe_create_indices call launches: one CTA does everything for
-    N <= 1024 slots; otherwise count + scatter, plus a scan kernel when the
-    count matrix (experts x 1024-slot chunks, rows padded to 4) exceeds 32Ki words."""
-    chunks = -(-num_slots // 1024)
-    if chunks <= 1:
-        return 1
-    row = (chunks + 3) // 4 * 4
-    return 2 if row * n_experts <= 32 * 1024 else 3
+    N <= 1024 slots; otherwise count, row prefixes and scatter."""
+    return 1 if num_slots <= 1024 else 3
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:

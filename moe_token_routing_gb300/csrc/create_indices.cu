@@ -9,21 +9,22 @@
 // here positions are computed arithmetically, so any count per expert works.
 //
 // Design (no inter-CTA waits, deterministic, stable):
-//   count   : CTA b counts the experts of its 1024 slots (warp-aggregated with
-//             match.any, shared-memory counters) -> counts[e][b] (expert-major,
-//             so one expert's counts are contiguous).
-//   scatter : CTA b derives its bases itself from the small count matrix:
-//             base[b][e] = start(e) + sum_{b' < b} counts[e][b'], with start(e)
-//             the exclusive sum of the per-expert totals; CTA 0 also writes the
-//             compact CSR, expert_ids, usage stats and the device status word.
-//             Then it re-reads its slots; within a CTA each warp owns 128
-//             consecutive slots, so a slot's position is base[b][e] + (slots of
-//             e in earlier warps) + (slots of e in earlier steps of its warp) +
+//   count   : CTA b counts the experts of its 1024 slots, one per thread
+//             (warp-aggregated with match.any, shared-memory counters) ->
+//             counts[e][b] (expert-major, so one expert's counts are
+//             contiguous).
+//   rows    : one warp per expert turns its row into exclusive prefixes,
+//             counts[e][b] := sum_{b' < b} counts[e][b'], and writes the total
+//             tot[e]; each warp instruction covers 128 consecutive counts.
+//   scatter : CTA b scans the totals into expert starts start(e) (CTA 0 also
+//             writes the compact CSR, expert_ids, usage stats and the device
+//             status word), reads its column of prefixes, and re-reads its
+//             slots; within a CTA each warp owns 128 consecutive slots, so a
+//             slot's position is start(e) + counts[e][b] + (slots of e in
+//             earlier warps) + (slots of e in earlier steps of its warp) +
 //             (lower lanes of its step with the same e). Writes
 //             token_expert_order and restore_token_order in one pass.
-//   For N <= 1024 one CTA does everything in one launch. When the count matrix
-//   is too large for every CTA to read it (more than 32Ki words), a one-CTA
-//   scan kernel turns the counts into bases in between.
+//   For N <= 1024 one CTA does everything in one launch.
 #include <mutex>
 
 #include "index_device.cuh"
@@ -32,116 +33,101 @@ namespace moe {
 namespace {
 
 constexpr size_t kHeaderBytes = 256;
+constexpr int kCountThreads = kSlotsPerCta;  // one slot per thread in the count kernel
+constexpr int kRowsWarps = 8;                // rows kernel: warps per CTA, one expert each
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-constexpr int64_t kMaxSharedCountWords = 32 * 1024;  // every scatter CTA reads them all
 
 struct Layout {
   int64_t num_blocks;
   int64_t row;  // words per expert row of the count matrix (num_blocks rounded up to 4)
-  size_t flags_off, counts_off, total;
+  size_t flags_off, counts_off, totals_off, total;
 };
 
+// Workspace: header (word 0: status) | flags [NB] | counts [E][row] | totals [E].
 Layout workspace_layout(int64_t N, int E) {
   Layout L;
   L.num_blocks = (N + kSlotsPerCta - 1) / kSlotsPerCta;
   L.row = (L.num_blocks + 3) & ~(int64_t)3;
   L.flags_off = kHeaderBytes;
   if (L.num_blocks <= 1) {
-    L.counts_off = kHeaderBytes;
+    L.counts_off = L.totals_off = kHeaderBytes;
     L.total = kHeaderBytes;
   } else {
     L.counts_off = L.flags_off + align256(sizeof(uint32_t) * (size_t)L.num_blocks);
-    L.total = L.counts_off + align256(sizeof(uint32_t) * (size_t)L.row * (size_t)E);
+    L.totals_off = L.counts_off + align256(sizeof(uint32_t) * (size_t)L.row * (size_t)E);
+    L.total = L.totals_off + align256(sizeof(uint32_t) * (size_t)E);
   }
   return L;
 }
 
 // ---------------------------------------------------------------- kernels
-__global__ void __launch_bounds__(kIdxThreads) idx_count_kernel(const IdxArgs a) {
+__global__ void __launch_bounds__(kCountThreads) idx_count_kernel(const IdxArgs a) {
   extern __shared__ uint32_t s_cnt[];  // [E]
   wait_for_prior_grid();
-  for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
-  int v[kStepsPerWarp];
+  const int lane = threadIdx.x & 31;
+  const int64_t i = (int64_t)blockIdx.x * kSlotsPerCta + threadIdx.x;
   bool bad = false;
-  load_warp_slots(a, warp_base, v, bad);
-#pragma unroll
-  for (int s = 0; s < kStepsPerWarp; ++s) {
-    const unsigned peers = __match_any_sync(kFullMask, v[s]);
-    if (v[s] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[v[s]], (uint32_t)__popc(peers));
+  int v = -1;
+  if (i < (int64_t)a.N) {
+    v = __ldg(a.ids + i);
+    if (v < 0 || v >= a.E) {
+      bad = true;
+      v = -1;
+    }
   }
+  const unsigned peers = __match_any_sync(kFullMask, v);
+  if (v >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[v], (uint32_t)__popc(peers));
   const int any_bad = __syncthreads_or(bad);
-  for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x)
     a.counts[(int64_t)e * a.row + blockIdx.x] = s_cnt[e];
   if (blockIdx.x == a.num_blocks - 1) {  // padding columns of the count rows
     const int pad = a.row - a.num_blocks;
-    for (int j = threadIdx.x; j < a.E * pad; j += kIdxThreads)
+    for (int j = threadIdx.x; j < a.E * pad; j += blockDim.x)
       a.counts[(int64_t)(j / pad) * a.row + a.num_blocks + j % pad] = 0u;
   }
   if (threadIdx.x == 0) a.flags[blockIdx.x] = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
 }
 
-__global__ void __launch_bounds__(kScanThreads) idx_scan_kernel(const IdxArgs a) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* part = smem;                      // [P][E] partial sums per block range
-  uint32_t* tot = part + kScanThreads;        // [E]
-  uint32_t* act = tot + MOE_MAX_EXPERTS;      // [E]
-  uint32_t* pad = act + MOE_MAX_EXPERTS;      // [E]
-  __shared__ uint32_t warp_tmp[32];
+// One warp per expert e: exclusive prefix of the row counts[e][0..row) in
+// place, 128 counts per pass (lane l takes counts 4l .. 4l+3 with one 16-byte
+// load), and the row total to totals[e]. The padding columns are zero.
+__global__ void __launch_bounds__(kRowsWarps * 32) idx_rows_kernel(const IdxArgs a) {
   wait_for_prior_grid();
-
-  const int E = a.E, NB = a.num_blocks;
-  const int P = max(1, kScanThreads / E);
-  const int e = threadIdx.x % E, p = threadIdx.x / E;
-  const bool worker = p < P;
-  const int b0 = worker ? (int)((int64_t)NB * p / P) : 0;
-  const int b1 = worker ? (int)((int64_t)NB * (p + 1) / P) : 0;
-
-  uint32_t sum = 0;
-#pragma unroll 8
-  for (int b = b0; b < b1; ++b) sum += a.counts[(int64_t)e * a.row + b];
-  if (worker) part[p * E + e] = sum;
-  __syncthreads();
-  if (threadIdx.x < E) {
-    uint32_t run = 0;
-    for (int q = 0; q < P; ++q) {
-      const uint32_t c = part[q * E + threadIdx.x];
-      part[q * E + threadIdx.x] = run;
-      run += c;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRowsWarps + (threadIdx.x >> 5);
+  if (e >= a.E) return;
+  uint4* row = reinterpret_cast<uint4*>(a.counts + (int64_t)e * a.row);
+  const int Q = a.row / 4;
+  uint32_t carry = 0;
+  for (int q0 = 0; q0 < Q; q0 += 32) {
+    const int q = q0 + lane;
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);
+    if (q < Q) c = row[q];
+    const uint32_t sum = c.x + c.y + c.z + c.w;
+    uint32_t incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += y;
     }
-    tot[threadIdx.x] = run;
+    uint4 o;
+    o.x = carry + incl - sum;
+    o.y = o.x + c.x;
+    o.z = o.y + c.y;
+    o.w = o.z + c.z;
+    if (q < Q) row[q] = o;
+    carry += __shfl_sync(kFullMask, incl, 31);
   }
-  __syncthreads();
-  emit_expert_table(a, tot, act, pad, warp_tmp);
-  __syncthreads();
-  if (worker) {
-    uint32_t base = tot[e] + part[p * E + e];
-    for (int b = b0; b < b1; ++b) {
-      const uint32_t c = a.counts[(int64_t)e * a.row + b];
-      a.counts[(int64_t)e * a.row + b] = base;
-      base += c;
-    }
-  }
-  __shared__ uint32_t s_flags;
-  if (threadIdx.x == 0) s_flags = 0;
-  __syncthreads();
-  uint32_t flags = 0;
-  for (int b = threadIdx.x; b < NB; b += kScanThreads) flags |= a.flags[b];
-  flags = __reduce_or_sync(kFullMask, flags);
-  if ((threadIdx.x & 31) == 0 && flags) atomicOr(&s_flags, flags);
-  __syncthreads();
-  if (threadIdx.x == 0) *a.status = s_flags;
+  if (lane == 0) a.totals[e] = carry;
 }
 
 // Where a scatter CTA takes its per-expert bases from.
 enum BaseSource : int {
   kBasesSingleCta = 0,  // one CTA covers all slots: the bases are the expert starts
-  kBasesFromCounts = 1, // each CTA sums the count matrix itself
-  kBasesFromScan = 2    // the scan kernel wrote them into the count matrix
+  kBasesFromCounts = 1  // the last count CTA wrote them into the count matrix
 };
 
 template <int kBases>
@@ -150,10 +136,8 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   uint32_t* s_warp = smem;                      // [kIdxWarps][E]
   uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
   uint32_t* s_act = s_base + a.E;               // [E]
-  uint32_t* s_pre = s_act + a.E;                // [E]
-  uint32_t* s_pad = s_pre + a.E;                // [E]
+  uint32_t* s_pad = s_act + a.E;                // [E]; s_pad + E: [E] prefixes
   __shared__ uint32_t warp_tmp[32];
-  __shared__ uint32_t s_flags;
   wait_for_prior_grid();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -185,25 +169,18 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
-  } else if constexpr (kBases == kBasesFromCounts) {
-    // totals and the prefix over earlier CTAs, from each expert's contiguous count row
+  } else {
+    // totals -> expert starts (CTA 0: the whole expert table and the status
+    // word), plus this CTA's column of prefixes over earlier CTAs
+    __shared__ uint32_t s_flags;
     const int b = blockIdx.x;
+    uint32_t* s_pre = s_pad + a.E;  // [E]
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-      const uint4* row = reinterpret_cast<const uint4*>(a.counts + (int64_t)e * a.row);
-      uint32_t tot = 0, pre = 0;
-#pragma unroll 16
-      for (int q = 0; q < a.row / 4; ++q) {
-        const uint4 c = row[q];
-        tot += c.x + c.y + c.z + c.w;
-        pre += (4 * q < b ? c.x : 0u) + (4 * q + 1 < b ? c.y : 0u) + (4 * q + 2 < b ? c.z : 0u) +
-               (4 * q + 3 < b ? c.w : 0u);
-      }
-      s_base[e] = tot;
-      s_pre[e] = pre;
+      s_base[e] = a.totals[e];
+      s_pre[e] = a.counts[(int64_t)e * a.row + b];
     }
     if (threadIdx.x == 0) s_flags = 0;
     __syncthreads();
-    // s_base[e] := start(e); only CTA 0 needs the rest of the expert table
     if (b == 0)
       emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
     else
@@ -217,9 +194,6 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
       __syncthreads();
       if (threadIdx.x == 0) *a.status = s_flags;
     }
-  } else {
-    for (int e = threadIdx.x; e < a.E; e += kIdxThreads)
-      s_base[e] = a.counts[(int64_t)e * a.row + blockIdx.x];
   }
   __syncthreads();
   // per-warp running offsets: base + slots of e in earlier warps
@@ -257,8 +231,6 @@ moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream
     if (cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromCounts>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
-        cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromScan>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
@@ -266,15 +238,11 @@ moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream
     return launch(idx_scatter_kernel<kBasesSingleCta>, 1, kIdxThreads, scatter_smem, stream, a);
   }
   moe_status_t st =
-      launch(idx_count_kernel, a.num_blocks, kIdxThreads, sizeof(uint32_t) * a.E, stream, a);
+      launch(idx_count_kernel, a.num_blocks, kCountThreads, sizeof(uint32_t) * a.E, stream, a);
   if (st != MOE_OK) return st;
-  if (L.row * a.E <= kMaxSharedCountWords)
-    return launch(idx_scatter_kernel<kBasesFromCounts>, a.num_blocks, kIdxThreads, scatter_smem,
-                  stream, a);
-  const size_t scan_smem = sizeof(uint32_t) * (kScanThreads + 3 * MOE_MAX_EXPERTS);
-  st = launch(idx_scan_kernel, 1, kScanThreads, scan_smem, stream, a);
+  st = launch(idx_rows_kernel, (a.E + kRowsWarps - 1) / kRowsWarps, kRowsWarps * 32, 0, stream, a);
   if (st != MOE_OK) return st;
-  return launch(idx_scatter_kernel<kBasesFromScan>, a.num_blocks, kIdxThreads, scatter_smem,
+  return launch(idx_scatter_kernel<kBasesFromCounts>, a.num_blocks, kIdxThreads, scatter_smem,
                 stream, a);
 }
 
@@ -322,6 +290,7 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   a.stats = expert_usage_stats;
   a.scales_offset = scales_offset_p;
   a.status = reinterpret_cast<uint32_t*>(ws);
+  a.totals = reinterpret_cast<uint32_t*>(ws + L.totals_off);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
   a.N = (uint32_t)N;
@@ -412,6 +381,7 @@ extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order
   a.stats = expert_usage_stats;
   a.scales_offset = nullptr;
   a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(ws);
+  a.totals = reinterpret_cast<uint32_t*>(ws + L.totals_off);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
   a.N = (uint32_t)N;

