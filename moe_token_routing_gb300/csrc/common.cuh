@@ -40,9 +40,15 @@ inline moe_status_t launch_status() {
 // Every kernel of the library starts with this: with programmatic dependent
 // launch the grid may begin while the previous kernel on the stream is still
 // finishing, and this waits until that kernel has completed and its writes are
-// visible. Without programmatic launch it returns at once.
+// visible. It then lets the next kernel on the stream be scheduled onto SMs
+// that this grid frees, so that its launch overlaps this grid's tail; that
+// kernel waits in turn before it reads anything. Because every kernel releases
+// its dependents only after its own wait, a kernel that has started knows
+// that every grid two or more launches back has completed. Without
+// programmatic launch both instructions return at once.
 __device__ __forceinline__ void wait_for_prior_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Launches `kernel` on `stream` with programmatic stream serialisation, so its

@@ -138,7 +138,11 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   uint32_t* s_act = s_base + a.E;               // [E]
   uint32_t* s_pad = s_act + a.E;                // [E]; s_pad + E: [E] prefixes
   __shared__ uint32_t warp_tmp[32];
-  wait_for_prior_grid();
+  // With the count matrix from the count and rows kernels, this kernel is the
+  // third of the call, so the ids (written before the count kernel ran) are
+  // complete once it starts: the warp counts overlap the rows kernel's tail.
+  // A single CTA runs right after the ids' producer and must wait first.
+  if constexpr (kBases == kBasesSingleCta) wait_for_prior_grid();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* my_cnt = s_warp + warp * a.E;
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
     __syncwarp();
   }
+  if constexpr (kBases == kBasesFromCounts) wait_for_prior_grid();  // counts, totals
   __syncthreads();
 
   if constexpr (kBases == kBasesSingleCta) {

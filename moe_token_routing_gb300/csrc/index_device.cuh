@@ -133,7 +133,7 @@ __device__ __forceinline__ void load_warp_slots(const IdxArgs& a, int64_t warp_b
     const int64_t i = warp_base + s * 32 + lane;
     int id = -1;
     if (i < (int64_t)a.N) {
-      id = __ldg(a.ids + i);
+      id = __ldcg(a.ids + i);
       if (id < 0 || id >= a.E) {
         bad = true;
         id = -1;
