@@ -16,9 +16,10 @@
 //   rows    : one warp per expert turns its row into exclusive prefixes,
 //             counts[e][b] := sum_{b' < b} counts[e][b'], and writes the total
 //             tot[e]; each warp instruction covers 128 consecutive counts.
-//   scatter : CTA b scans the totals into expert starts start(e) (CTA 0 also
-//             writes the compact CSR, expert_ids, usage stats and the device
-//             status word), reads its column of prefixes, and re-reads its
+//   scatter : CTA b scans the totals into expert starts start(e) and writes
+//             its share of the compact CSR, expert_ids and scale offsets (CTA
+//             0 also the usage stats and the device status word), reads its
+//             column of prefixes, and re-reads its
 //             slots; within a CTA each warp owns 128 consecutive slots, so a
 //             slot's position is start(e) + counts[e][b] + (slots of e in
 //             earlier warps) + (slots of e in earlier steps of its warp) +
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   uint32_t* s_warp = smem;                      // [kIdxWarps][E]
   uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
   uint32_t* s_act = s_base + a.E;               // [E]
-  uint32_t* s_pad = s_act + a.E;                // [E]; s_pad + E: [E] prefixes
+  uint32_t* s_pad = s_act + a.E;                // [E]; then [E] totals, [E] prefixes
   __shared__ uint32_t warp_tmp[32];
   // With the count matrix from the count and rows kernels, this kernel is the
   // third of the call, so the ids (written before the count kernel ran) are
@@ -175,21 +176,21 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
   } else {
-    // totals -> expert starts (CTA 0: the whole expert table and the status
-    // word), plus this CTA's column of prefixes over earlier CTAs
+    // totals -> expert starts, active and padded offsets in one pass; every
+    // CTA writes its share of the expert table and CTA 0 the status word;
+    // then base = start + this CTA's column of prefixes over earlier CTAs
     __shared__ uint32_t s_flags;
     const int b = blockIdx.x;
-    uint32_t* s_pre = s_pad + a.E;  // [E]
+    uint32_t* s_tot = s_pad + a.E;  // [E]
+    uint32_t* s_pre = s_tot + a.E;  // [E]
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-      s_base[e] = a.totals[e];
+      s_tot[e] = a.totals[e];
       s_pre[e] = a.counts[(int64_t)e * a.row + b];
     }
     if (threadIdx.x == 0) s_flags = 0;
     __syncthreads();
-    if (b == 0)
-      emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
-    else
-      block_exclusive_scan(s_base, a.E, warp_tmp);
+    const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
+    write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
     if (b == 0) {
       uint32_t f = 0;
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
 }
 
 moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream) {
-  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 4) * a.E;
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * a.E;
   if (scatter_smem > 40 * 1024) {  // large E: opt in above the default 48 KB block limit
     const int bytes = (int)scatter_smem;
     if (cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,

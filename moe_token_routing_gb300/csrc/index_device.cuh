@@ -124,6 +124,111 @@ __device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act
   }
 }
 
+// Sums that the expert table needs besides the per-expert arrays.
+struct TableSums {
+  uint32_t active, padded_total, max_count;
+};
+
+// From tot[0..E) (shared memory), every thread of the block computes, in one
+// pass of a blocked scan: start[e] (slots before expert e), act[e] (active
+// experts before e), pad[e] (128-row padded slots before e), and the sums.
+__device__ TableSums scan_expert_table(const uint32_t* tot, uint32_t* start, uint32_t* act,
+                                       uint32_t* pad, int E) {
+  __shared__ uint4 w_sum[32];
+  __shared__ uint4 s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const int per = (E + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int beg = min((int)threadIdx.x * per, E), end = min(beg + per, E);
+  uint32_t st = 0, ac = 0, pd = 0, mx = 0;
+  for (int e = beg; e < end; ++e) {
+    const uint32_t c = tot[e];
+    st += c;
+    ac += c > 0u;
+    pd += (c + (kScaleRowAlign - 1)) / kScaleRowAlign * kScaleRowAlign;
+    mx = max(mx, c);
+  }
+  uint32_t ist = st, iac = ac, ipd = pd;  // inclusive warp scans
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t a0 = __shfl_up_sync(kFullMask, ist, off);
+    const uint32_t a1 = __shfl_up_sync(kFullMask, iac, off);
+    const uint32_t a2 = __shfl_up_sync(kFullMask, ipd, off);
+    if (lane >= off) {
+      ist += a0;
+      iac += a1;
+      ipd += a2;
+    }
+  }
+  const uint32_t wmax = __reduce_max_sync(kFullMask, mx);
+  if (lane == 31) w_sum[warp] = make_uint4(ist, iac, ipd, wmax);
+  __syncthreads();
+  if (warp == 0) {
+    uint4 v = lane < nwarps ? w_sum[lane] : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t x = v.x, y = v.y, z = v.z;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t a0 = __shfl_up_sync(kFullMask, x, off);
+      const uint32_t a1 = __shfl_up_sync(kFullMask, y, off);
+      const uint32_t a2 = __shfl_up_sync(kFullMask, z, off);
+      if (lane >= off) {
+        x += a0;
+        y += a1;
+        z += a2;
+      }
+    }
+    const uint32_t m = __reduce_max_sync(kFullMask, v.w);
+    w_sum[lane] = make_uint4(x - v.x, y - v.y, z - v.z, 0u);  // exclusive over warps
+    if (lane == 31) s_total = make_uint4(x, y, z, m);
+  }
+  __syncthreads();
+  const uint4 wb = w_sum[warp];
+  uint32_t rst = wb.x + ist - st, rac = wb.y + iac - ac, rpd = wb.z + ipd - pd;
+  for (int e = beg; e < end; ++e) {
+    const uint32_t c = tot[e];
+    start[e] = rst;
+    act[e] = rac;
+    pad[e] = rpd;
+    rst += c;
+    rac += c > 0u;
+    rpd += (c + (kScaleRowAlign - 1)) / kScaleRowAlign * kScaleRowAlign;
+  }
+  const uint4 t = s_total;
+  __syncthreads();
+  TableSums r;
+  r.active = t.y;
+  r.padded_total = t.z;
+  r.max_count = t.w;
+  return r;
+}
+
+// This CTA's share of the expert table (compact CSR, expert_ids, the
+// optional scale offsets; CTA 0 also the usage stats): experts [E*b/B,
+// E*(b+1)/B) and tail entries [A + (E+1-A)*b/B, A + (E+1-A)*(b+1)/B).
+__device__ void write_table_share(const IdxArgs& a, const uint32_t* tot, const uint32_t* start,
+                                  const uint32_t* act, const uint32_t* pad, const TableSums& t) {
+  const int E = a.E, B = gridDim.x, b = blockIdx.x;
+  const int e0 = (int)((int64_t)E * b / B), e1 = (int)((int64_t)E * (b + 1) / B);
+  for (int e = e0 + (int)threadIdx.x; e < e1; e += blockDim.x) {
+    if (tot[e] > 0u) {
+      a.expert_ids[act[e]] = e;
+      a.expert_start_indices[act[e]] = start[e];
+      if (a.scales_offset) a.scales_offset[act[e]] = pad[e];
+    }
+  }
+  const int64_t A = t.active, tail = (int64_t)E + 1 - A;
+  const int j0 = (int)(A + tail * b / B), j1 = (int)(A + tail * (b + 1) / B);
+  for (int j = j0 + (int)threadIdx.x; j < j1; j += blockDim.x) {
+    a.expert_start_indices[j] = a.N;
+    if (j < E) a.expert_ids[j] = -1;
+    if (a.scales_offset) a.scales_offset[j] = t.padded_total;
+  }
+  if (b == 0 && threadIdx.x == 0) {
+    a.stats[0] = t.max_count;
+    a.stats[1] = t.active;
+  }
+}
+
 // Loads this warp's slots: -1 marks a slot past N or an id outside [0, E).
 __device__ __forceinline__ void load_warp_slots(const IdxArgs& a, int64_t warp_base,
                                                 int (&v)[kStepsPerWarp], bool& bad) {
