@@ -169,3 +169,13 @@ def test_one_workspace_across_sizes_and_done_counter_left_zero():
                               ref["restore_token_order"])
         assert np.array_equal(bufs.expert_start_indices.cpu().numpy().view(np.uint32),
                               ref["expert_start_indices"])
+
+
+@pytest.mark.parametrize("N,E", [(3_000_001, 64), (600_000, 1024)])
+def test_long_count_rows(N, E):
+    """Count rows longer than one 128-count pass of the row-prefix kernel (2930
+    and 586 CTAs), with a skewed expert mix."""
+    rng = np.random.default_rng(N + E)
+    ids = rng.integers(0, E, size=N).astype(np.int32)
+    ids[::3] = rng.integers(0, 4, size=ids[::3].size)
+    assert_index_parity(ids, E)
