@@ -411,6 +411,14 @@ def run_gpu(args, cfg, rank, world, local_rank):
         pev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     sig_ms = statistics.fmean([e[0].elapsed_time(e[1]) for e in pev])
+    for i in range(kp):
+        flush_l2()
+        pev[i][0].record(stream)
+        moe.moe_route_ex(ids_x, w_x, logits_d, b_d, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                         moe.SCORES_SOFTMAX)
+        pev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    soft_ms = statistics.fmean([e[0].elapsed_time(e[1]) for e in pev])
 
     # ---- end to end through the host-buffer API: pinned inputs copied in and the
     # output copied back every step, copies of consecutive steps overlapped
@@ -493,7 +501,12 @@ def run_gpu(args, cfg, rank, world, local_rank):
                 "ms": sig_ms, "tokens_per_s": cfg.T / (sig_ms * 1e-3),
                 "achieved_gbs": nbytes["route"] / (sig_ms * 1e-3) / 1e9,
                 "note": "moe_route_ex with the fused sigmoid loader on gate logits; "
-                        "same bytes as route"}},
+                        "same bytes as route"},
+            "route_softmax_logits": {
+                "ms": soft_ms, "tokens_per_s": cfg.T / (soft_ms * 1e-3),
+                "achieved_gbs": nbytes["route"] / (soft_ms * 1e-3) / 1e9,
+                "note": "moe_route_ex with the fused softmax loader on gate logits (sum over "
+                        "experts in ascending order); same bytes as route"}},
         "stages_tokens_per_s": {"route": cfg.T / (route_mean * 1e-3),
                                 "create_indices": cfg.T / (statistics.fmean(index_ms) * 1e-3),
                                 "finalize": cfg.T / (fin_mean * 1e-3)},

@@ -105,7 +105,8 @@ moe_status_t moe_route(int32_t* expert_indices, float* expert_weights,
 /* Score loaders of moe_route_ex (the page's scores_input_fn). */
 typedef enum {
   MOE_SCORES_AS_GIVEN = 0, /* the score is the loaded value (moe_route) */
-  MOE_SCORES_SIGMOID = 1   /* the score is sigmoid(loaded logit) */
+  MOE_SCORES_SIGMOID = 1,  /* the score is sigmoid(loaded logit) */
+  MOE_SCORES_SOFTMAX = 2   /* the scores are the softmax of the token's logits */
 } moe_score_fn_t;
 
 /*
@@ -121,6 +122,10 @@ typedef enum {
  * reduction by ln2 (head 0.693145751953125, tail 1.42860682030941723e-6),
  * degree-7 Taylor polynomial in Horner form with fused multiply-adds, times
  * 2^n; within a few ulp of the true value, and reproducible bit for bit.
+ * With MOE_SCORES_SOFTMAX, the scores of a token are the softmax of its E
+ * logits, exp(x - max) / sum, with that exp, fp32 throughout, and the sum taken
+ * in ascending expert order (the plainest reading: the page gives no order),
+ * so the result is reproducible bit for bit as well.
  * Everything else is as in moe_route. An unknown score_fn returns
  * MOE_ERR_UNSUPPORTED.
  */

@@ -7,7 +7,7 @@ route_index runs the first two as one cooperative launch.
 """
 from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_SYNC_STATE,
                       DEVICE_STATUS_SYNC_TIMEOUT, EXPORTED_SYMBOLS, SCORES_AS_GIVEN,
-                      SCORES_SIGMOID, IndexBuffers, MoeError, MoeLibraryMissing,
+                      SCORES_SIGMOID, SCORES_SOFTMAX, IndexBuffers, MoeError, MoeLibraryMissing,
                       RouteIndexBuffers, create_indices, finalize, load_library,
                       moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
                       moe_finalize_ex, moe_permute, moe_read_device_status, moe_route,
@@ -22,5 +22,5 @@ __all__ = [
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
     "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
     "moe_finalize_ex", "moe_permute", "moe_read_device_status", "moe_route", "moe_route_ex",
-    "permute", "route", "SCORES_AS_GIVEN", "SCORES_SIGMOID",
+    "permute", "route", "SCORES_AS_GIVEN", "SCORES_SIGMOID", "SCORES_SOFTMAX",
 ]

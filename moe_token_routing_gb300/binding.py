@@ -130,6 +130,7 @@ def moe_route(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
 
 SCORES_AS_GIVEN = 0
 SCORES_SIGMOID = 1
+SCORES_SOFTMAX = 2
 
 
 def moe_route_ex(expert_indices: torch.Tensor, expert_weights: torch.Tensor,

@@ -22,13 +22,13 @@
 namespace moe {
 namespace {
 
-template <int C, bool kVec>
+template <int C, bool kVec, bool kSoftmax>
 __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kernel(const RouteArgs a) {
-  extern __shared__ float dyn_smem[];  // kGroupsGeneric: kRouteWarps * E biased scores
+  extern __shared__ float dyn_smem[];  // kRouteWarps * a.warp_smem_words
   wait_for_prior_grid();
   const int warp = threadIdx.x >> 5;
-  route_tokens_warp<C, kVec>(a, (int64_t)blockIdx.x * kRouteWarps + warp, a.T,
-                             (int64_t)gridDim.x * kRouteWarps, dyn_smem + warp * a.E,
+  route_tokens_warp<C, kVec, kSoftmax>(a, (int64_t)blockIdx.x * kRouteWarps + warp, a.T,
+                             (int64_t)gridDim.x * kRouteWarps, dyn_smem + warp * a.warp_smem_words,
                              [](int64_t, int, int) {});
 }
 
@@ -62,13 +62,20 @@ moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, 
   return launch(k, grid, kRouteThreads, smem, stream, a);
 }
 
+template <int C, bool kSoftmax>
+moe_status_t launch_warp_path_fn(const RoutePlan& p, cudaStream_t stream) {
+  const size_t smem = route_warp_smem(p, kRouteWarps);
+  if constexpr (C % 4 == 0) {
+    if (p.vec)
+      return launch_route(route_warp_kernel<C, true, kSoftmax>, p.a, kRouteWarps, smem, stream);
+  }
+  return launch_route(route_warp_kernel<C, false, kSoftmax>, p.a, kRouteWarps, smem, stream);
+}
+
 template <int C>
 moe_status_t launch_warp_path(const RoutePlan& p, cudaStream_t stream) {
-  const size_t smem = route_group_smem(p);
-  if constexpr (C % 4 == 0) {
-    if (p.vec) return launch_route(route_warp_kernel<C, true>, p.a, kRouteWarps, smem, stream);
-  }
-  return launch_route(route_warp_kernel<C, false>, p.a, kRouteWarps, smem, stream);
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_warp_path_fn<C, true>(p, stream);
+  return launch_warp_path_fn<C, false>(p, stream);
 }
 
 template <int EP>

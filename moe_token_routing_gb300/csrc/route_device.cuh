@@ -38,6 +38,10 @@ struct RouteArgs {
   int group_mode;
   int seg_lanes;  // lanes per group in kGroupsSegment
   int score_fn;   // moe_score_fn_t applied to every loaded score
+  // Warp path: floats of shared memory per warp: E for the generic group
+  // layout's biased scores, then E for the token's softmax scores.
+  int warp_smem_words;
+  int softmax_off;
 };
 
 // exp(x) in fp32 by Cody-Waite range reduction (W. J. Cody and W. Waite,
@@ -63,7 +67,8 @@ __device__ __forceinline__ float score_exp_f32(float x) {
   return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
 }
 
-// The page's scores_input_fn: the score of (token, expert) from the loaded value.
+// The page's scores_input_fn for the element-wise loaders: the score of
+// (token, expert) from the loaded value.
 __device__ __forceinline__ float apply_score_fn(int fn, float x) {
   if (fn == MOE_SCORES_SIGMOID) return __fdiv_rn(1.0f, __fadd_rn(1.0f, score_exp_f32(-x)));
   return x;
@@ -139,13 +144,53 @@ __device__ __forceinline__ int select_by_full_rounds(uint32_t (&key)[C], int lan
   return my_id;
 }
 
+// The softmax loader on one token's logits, held C per lane (lane l: experts
+// l*C .. l*C+C-1): s := exp(s - max) / sum, with the sum taken in ascending
+// expert order (each lane adds its experts to the running sum of the lanes
+// before it), so the result is bit-identical to a sequential loop. The scores
+// are also left in `strip` (E floats) for the weights.
+template <int C>
+__device__ __forceinline__ void softmax_lane_row(const RouteArgs& a, float (&s)[C],
+                                                 const bool (&valid)[C], int lane, int e0,
+                                                 float* strip) {
+  float m = -CUDART_INF_F;
+#pragma unroll
+  for (int c = 0; c < C; ++c)
+    if (valid[c]) m = fmaxf(m, s[c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
+  float ex[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) ex[c] = valid[c] ? score_exp_f32(__fsub_rn(s[c], m)) : 0.0f;
+  const int lanes = (a.E + C - 1) / C;
+  float run = 0.0f;
+  for (int l = 0; l < lanes; ++l) {
+    if (lane == l) {
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        if (valid[c]) run = __fadd_rn(run, ex[c]);
+    }
+    run = __shfl_sync(kFullMask, run, l);
+  }
+  __syncwarp();  // the previous token's weights have been read from the strip
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    s[c] = valid[c] ? __fdiv_rn(ex[c], run) : 0.0f;
+    if (valid[c]) strip[e0 + c] = s[c];
+  }
+  __syncwarp();
+}
+
 // Routes tokens first, first + stride, ... (below end) with the calling warp.
-// Lane l holds experts l*C .. l*C+C-1. `group_smem` is this warp's E floats of
-// shared memory (used by kGroupsGeneric only). After token t's ids and weights
-// are written, lane k < K calls on_id(t, k, id).
-template <int C, bool kVec, typename OnId>
+// Lane l holds experts l*C .. l*C+C-1. `warp_smem` is this warp's
+// a.warp_smem_words floats of shared memory (the generic group layout's
+// biased scores, the softmax loader's scores). After token t's ids and
+// weights are written, lane k < K calls on_id(t, k, id). kSoftmax selects the
+// softmax loader (a separate instantiation keeps the other loaders' register
+// budget).
+template <int C, bool kVec, bool kSoftmax, typename OnId>
 __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t first, int64_t end,
-                                                  int64_t stride, float* group_smem,
+                                                  int64_t stride, float* warp_smem,
                                                   OnId on_id) {
   static_assert(C >= 2, "the warp path holds at least two experts per lane");
 
@@ -173,7 +218,9 @@ __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t fi
 #pragma unroll
     for (int c = 0; c < C; ++c) s[c] = s_next[c];
     if (t + stride < end) load_lane_scores<C, kVec>(a, t + stride, e0, valid, s_next);
-    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+    if constexpr (kSoftmax) {
+      softmax_lane_row<C>(a, s, valid, lane, e0, warp_smem + a.softmax_off);
+    } else if (a.score_fn != MOE_SCORES_AS_GIVEN) {
 #pragma unroll
       for (int c = 0; c < C; ++c) s[c] = apply_score_fn(a.score_fn, s[c]);
     }
@@ -185,7 +232,7 @@ __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t fi
     int my_id = 0;
     if (a.group_mode == kGroupsGeneric) {
       // ---- groups through shared memory, then the exact full-round selection ----
-      float* wb = group_smem;
+      float* wb = warp_smem;
 #pragma unroll
       for (int c = 0; c < C; ++c)
         if (valid[c]) wb[e0 + c] = b[c];
@@ -304,7 +351,13 @@ __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t fi
 
     // ---- weights: unbiased score, optional normalisation, scaling ----
     const float* row = a.scores + t * a.E;
-    float w = (lane < a.K) ? apply_score_fn(a.score_fn, __ldg(row + my_id)) : 0.0f;
+    float w = 0.0f;
+    if (lane < a.K) {
+      if constexpr (kSoftmax)  // (an id outside [0, E) is possible only for NaN scores)
+        w = (unsigned)my_id < (unsigned)a.E ? warp_smem[a.softmax_off + my_id] : 0.0f;
+      else
+        w = apply_score_fn(a.score_fn, __ldg(row + my_id));
+    }
     if (a.norm) {
       float sum = 0.0f;
 #pragma unroll 8
@@ -356,7 +409,21 @@ __device__ __forceinline__ void route_tokens_thread(const RouteArgs& a, int64_t 
 #pragma unroll
       for (int e = 0; e < EP; ++e) s[e] = ((valid >> e) & 1u) ? __ldg(row + e) : 0.0f;
     }
-    if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+    if (a.score_fn == MOE_SCORES_SOFTMAX) {
+      // exp(s - max) / sum, the sum in ascending expert order
+      float m = -CUDART_INF_F;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if ((valid >> e) & 1u) m = fmaxf(m, s[e]);
+      float sum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        s[e] = ((valid >> e) & 1u) ? score_exp_f32(__fsub_rn(s[e], m)) : 0.0f;
+        if ((valid >> e) & 1u) sum = __fadd_rn(sum, s[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < EP; ++e) s[e] = ((valid >> e) & 1u) ? __fdiv_rn(s[e], sum) : 0.0f;
+    } else if (a.score_fn != MOE_SCORES_AS_GIVEN) {
 #pragma unroll
       for (int e = 0; e < EP; ++e) s[e] = apply_score_fn(a.score_fn, s[e]);
     }
@@ -456,7 +523,8 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   if (E > MOE_MAX_EXPERTS || G > MOE_MAX_GROUPS || K > MOE_MAX_EXPERTS_PER_TOK)
     return MOE_ERR_UNSUPPORTED;
   if (num_tokens > (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
-  if (score_fn != MOE_SCORES_AS_GIVEN && score_fn != MOE_SCORES_SIGMOID)
+  if (score_fn != MOE_SCORES_AS_GIVEN && score_fn != MOE_SCORES_SIGMOID &&
+      score_fn != MOE_SCORES_SOFTMAX)
     return MOE_ERR_UNSUPPORTED;
 
   RouteArgs& a = p->a;
@@ -475,6 +543,8 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   a.group_mode = kGroupsAllKept;
   a.seg_lanes = 1;
   a.score_fn = score_fn;
+  a.warp_smem_words = 0;
+  a.softmax_off = 0;
   p->vec = (E % 4 == 0) && aligned(expert_scores, 16);
   p->C = 0;
   p->EP = E <= 8 ? 8 : E <= 16 ? 16 : 32;
@@ -489,6 +559,8 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
       a.group_mode = kGroupsGeneric;
     }
   }
+  a.softmax_off = a.group_mode == kGroupsGeneric ? E : 0;
+  a.warp_smem_words = a.softmax_off + (score_fn == MOE_SCORES_SOFTMAX ? E : 0);
   return MOE_OK;
 }
 
@@ -500,9 +572,9 @@ inline moe_status_t check_route_pointers(const RouteArgs& a) {
   return MOE_OK;
 }
 
-// Shared memory of the warp path's generic group layout: E floats per warp.
-inline size_t route_group_smem(const RoutePlan& p) {
-  return p.a.group_mode == kGroupsGeneric ? (size_t)kRouteWarps * p.a.E * sizeof(float) : 0;
+// Shared memory of the warp path for `warps` warps (RouteArgs.warp_smem_words each).
+inline size_t route_warp_smem(const RoutePlan& p, int warps) {
+  return (size_t)warps * p.a.warp_smem_words * sizeof(float);
 }
 
 }  // namespace

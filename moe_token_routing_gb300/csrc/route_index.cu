@@ -361,7 +361,7 @@ __host__ __device__ constexpr int thread_kernel_warps() {
   return EP <= 8 ? 32 : (EP <= 16 ? 16 : 8);
 }
 
-template <int C, bool kVec>
+template <int C, bool kVec, bool kSoftmax>
 __global__ void __launch_bounds__(warp_kernel_warps<C>() * 32, 1)
     route_index_warp_kernel(const FusedArgs f) {
   extern __shared__ __align__(16) uint32_t dyn[];
@@ -378,7 +378,8 @@ __global__ void __launch_bounds__(warp_kernel_warps<C>() * 32, 1)
   uint32_t* cta_cnt = m.s_cnt;
   if (tw0 < tw1) {
     // the work area holds the generic group layout's scores during routing
-    route_tokens_warp<C, kVec>(f.r, tw0, tw1, 1, reinterpret_cast<float*>(m.work) + warp * E,
+    route_tokens_warp<C, kVec, kSoftmax>(f.r, tw0, tw1, 1,
+                               reinterpret_cast<float*>(m.work) + warp * f.r.warp_smem_words,
                                [&](int64_t, int, int id) { count_expert(warp_cnt, cta_cnt, id, E); });
   }
   __syncthreads();
@@ -460,19 +461,26 @@ moe_status_t launch_fused(Kernel k, FusedArgs f, int warps, int64_t tokens_per_c
 size_t fused_smem(const RoutePlan& p, int warps) {
   const size_t E = (size_t)p.a.E;
   size_t work = 5 * E;  // totals, prefixes, starts, active and padded offsets
-  if (p.a.group_mode == kGroupsGeneric && work < (size_t)warps * E)
-    work = (size_t)warps * E;  // one row of biased scores per routing warp
+  const size_t routing = route_warp_smem(p, warps) / sizeof(uint32_t);
+  if (work < routing) work = routing;  // the routing warps' shared memory
   return sizeof(uint32_t) * ((size_t)(warps + 1) * E + work);
+}
+
+template <int C, bool kSoftmax>
+moe_status_t launch_fused_warp_fn(const RoutePlan& p, const FusedArgs& f, cudaStream_t stream) {
+  constexpr int W = warp_kernel_warps<C>();
+  const size_t smem = fused_smem(p, W);
+  if constexpr (C % 4 == 0) {
+    if (p.vec)
+      return launch_fused(route_index_warp_kernel<C, true, kSoftmax>, f, W, W, smem, stream);
+  }
+  return launch_fused(route_index_warp_kernel<C, false, kSoftmax>, f, W, W, smem, stream);
 }
 
 template <int C>
 moe_status_t launch_fused_warp(const RoutePlan& p, const FusedArgs& f, cudaStream_t stream) {
-  constexpr int W = warp_kernel_warps<C>();
-  const size_t smem = fused_smem(p, W);
-  if constexpr (C % 4 == 0) {
-    if (p.vec) return launch_fused(route_index_warp_kernel<C, true>, f, W, W, smem, stream);
-  }
-  return launch_fused(route_index_warp_kernel<C, false>, f, W, W, smem, stream);
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_fused_warp_fn<C, true>(p, f, stream);
+  return launch_fused_warp_fn<C, false>(p, f, stream);
 }
 
 template <int EP>

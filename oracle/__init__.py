@@ -51,9 +51,10 @@ def _open(path: str):
     lib.oracle_permute.argtypes = [vp, vp, i64, i32, i64, vp]
     lib.oracle_scales_offsets.argtypes = [vp, i64, i32, ctypes.c_uint32, vp]
     lib.oracle_sigmoid.argtypes = [vp, i64, vp]
+    lib.oracle_softmax.argtypes = [vp, i64, i32, vp]
     for f in (lib.oracle_route, lib.oracle_create_indices, lib.oracle_finalize,
               lib.oracle_finalize_tokens, lib.oracle_finalize_f64, lib.oracle_permute,
-              lib.oracle_scales_offsets, lib.oracle_sigmoid):
+              lib.oracle_scales_offsets, lib.oracle_sigmoid, lib.oracle_softmax):
         f.restype = ctypes.c_int
     return lib
 
@@ -180,3 +181,13 @@ def sigmoid(x):
     out = np.empty_like(a)
     _check(_load().oracle_sigmoid(ap, a.size, out.ctypes.data), "oracle_sigmoid")
     return out
+
+
+def softmax(x):
+    """fp32 softmax score loader over the last axis of a [rows, E] array."""
+    a, ap = _c(x, np.float32)
+    a2 = a.reshape(-1, a.shape[-1])
+    out = np.empty_like(a2)
+    _check(_load().oracle_softmax(ap, a2.shape[0], a2.shape[1], out.ctypes.data),
+           "oracle_softmax")
+    return out.reshape(a.shape)

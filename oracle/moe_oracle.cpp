@@ -52,6 +52,30 @@ extern "C" int oracle_sigmoid(const float* x, int64_t n, float* out) {
   return ORACLE_OK;
 }
 
+// group_limited_router_kernel, Parameters scores_input_fn: here the scores of
+// one token's gate logits x[0..E) are their softmax, exp(x_e - max x) divided
+// by the sum of those exponentials; the sum is taken in ascending expert
+// order. All in fp32 with the exp above.
+extern "C" int oracle_softmax(const float* x, int64_t rows, int32_t cols, float* out) {
+  if (rows < 0 || cols <= 0) return ORACLE_ERR_ARG;
+  std::vector<float> ex(cols);
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* row = x + r * cols;
+    float m = row[0];
+    for (int32_t e = 0; e < cols; ++e) {
+      if (std::isnan(row[e])) return ORACLE_ERR_NAN;
+      if (row[e] > m) m = row[e];
+    }
+    float sum = 0.0f;
+    for (int32_t e = 0; e < cols; ++e) {
+      ex[e] = exp_cody_waite(row[e] - m);
+      sum += ex[e];
+    }
+    for (int32_t e = 0; e < cols; ++e) out[r * cols + e] = ex[e] / sum;
+  }
+  return ORACLE_OK;
+}
+
 // group_limited_router_kernel, description paragraph: experts are split into
 // n_groups groups, the topk_group best groups are kept, and the
 // n_experts_per_tok experts are chosen from the kept groups; the bias is added

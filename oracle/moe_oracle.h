@@ -15,8 +15,8 @@
  *     expert_usage_stats, topk_ids).
  *   - "moe_finalize": description paragraph; Args (output, down,
  *     restore_order, router_weight).
- *   - "group_limited_router_kernel", Parameters scores_input_fn: a sigmoid
- *     score loader for gate logits;
+ *   - "group_limited_router_kernel", Parameters scores_input_fn: sigmoid and
+ *     softmax score loaders for gate logits;
  *   - the expert-contiguous token rows that the grouped matmul consumes
  *     ("moe_create_indices", description paragraph).
  *
@@ -61,6 +61,11 @@ extern "C" {
 /* Sigmoid score loader: out[i] = 1 / (1 + exp(-x[i])) in fp32, with exp by
  * Cody-Waite reduction and a degree-7 Taylor polynomial (see the .cpp). */
 int oracle_sigmoid(const float* x, int64_t n, float* out);
+
+/* Softmax score loader (Parameters scores_input_fn): out[r, e] =
+ * exp(x[r, e] - max_e' x[r, e']) / sum_e' exp(x[r, e'] - max), fp32, the sum
+ * in ascending e, exp as for oracle_sigmoid. */
+int oracle_softmax(const float* x, int64_t rows, int32_t cols, float* out);
 
 /* Router. scores [T,E] fp32 row-major, bias [E] fp32.
  * ids_out [T,K] int32, w_out [T,K] fp32. */

@@ -103,6 +103,7 @@ def test_route_ex_host_validation(lib):
     f = lib.moe_route_ex
     ok = (FAKE, FAKE, FAKE, FAKE)
     assert f(*ok, 4, 256, 8, 8, 4, 1, 1.0, 7, None) == 4      # unknown score loader
+    assert f(*ok, 4, 256, 8, 8, 4, 1, 1.0, 3, None) == 4
     assert f(*ok, 4, 256, 8, 7, 4, 1, 1.0, 1, None) == 2      # E % n_groups
     assert f(None, None, None, None, 0, 256, 8, 8, 4, 1, 1.0, 1, None) == 0
 

@@ -187,3 +187,47 @@ def test_sigmoid_loader_shapes_and_extremes(E, G, M, K):
     ids, w = gpu_route_sigmoid(logits, bias, K, G, M, True, 2.5)
     assert np.array_equal(ids, ids_ref)
     assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
+def gpu_route_softmax(logits, bias, K, G, M, norm, scale):
+    import moe_token_routing_gb300 as moe
+    s = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+    b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
+    T = logits.shape[0]
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route_ex(ids, w, s, b, G, M, norm, scale, moe.SCORES_SOFTMAX)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_softmax_loader_on_workloads(name):
+    """Parameters scores_input_fn: routing gate logits with the fused softmax
+    equals routing the oracle's softmax of the same logits, bit for bit (the
+    sum over experts in ascending order on both sides)."""
+    cfg = synth.get_config(name)
+    logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
+    bias = synth.make_bias(cfg)
+    ids_ref, w_ref = oracle.route(oracle.softmax(logits), bias, cfg.K, cfg.G, cfg.M,
+                                  cfg.norm_weights, cfg.scale)
+    ids, w = gpu_route_softmax(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    assert np.array_equal(ids, ids_ref)
+    assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,G,M,K", [(8, 4, 2, 3), (12, 3, 2, 4), (32, 4, 2, 8), (48, 4, 2, 6),
+                                     (96, 4, 2, 8), (120, 5, 2, 8), (256, 8, 4, 8),
+                                     (384, 1, 1, 8), (1024, 32, 4, 8)])
+@pytest.mark.parametrize("norm", [True, False])
+def test_softmax_loader_shapes_and_extremes(E, G, M, K, norm):
+    rng = np.random.default_rng(E + K + norm)
+    logits = (rng.standard_normal((300, E)) * 4).astype(np.float32)
+    logits[::7, ::3] = 90.0      # very large logits (exp needs the max shift)
+    logits[1::7, :] = -5.0       # all-equal rows
+    logits[2::7, ::5] = -150.0   # exp underflow clamp
+    bias = (rng.standard_normal(E) * 0.01).astype(np.float32)
+    ids_ref, w_ref = oracle.route(oracle.softmax(logits), bias, K, G, M, norm, 2.5)
+    ids, w = gpu_route_softmax(logits, bias, K, G, M, norm, 2.5)
+    assert np.array_equal(ids, ids_ref)
+    assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))

@@ -249,3 +249,17 @@ def test_fused_pipeline_matches_separate_launches():
     assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
     assert torch.equal(outs[0][1], outs[1][1])
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "skewed_ungrouped", "few_expert_large_batch"])
+def test_softmax_loader(name):
+    cfg = synth.get_config(name)
+    logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
+    bias = synth.make_bias(cfg)
+    ids_ref, w_ref = oracle.route(oracle.softmax(logits), bias, cfg.K, cfg.G, cfg.M,
+                                  cfg.norm_weights, cfg.scale)
+    idx_ref = oracle.create_indices(ids_ref, cfg.E)
+    moe = _moe()
+    got, _ = gpu_route_index(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                             score_fn=moe.SCORES_SOFTMAX)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)

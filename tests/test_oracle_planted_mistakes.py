@@ -18,6 +18,7 @@ import test_oracle_permute as tp
 import test_oracle_route as tr
 import test_oracle_scales as tsc
 import test_oracle_sigmoid as tsg
+import test_oracle_softmax as tsm
 
 ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
 
@@ -63,6 +64,10 @@ MUTANTS = {
                                     "for (int k = 6; k >= 1; --k) p = std::fma(p, r, inv_fact[k]);"),
     "sigmoid without the ln2 tail": ("r = std::fma(-n, 1.42860682030941723e-6f, r);", "r = r;"),
     "permute takes slot modulo K": ("const int64_t t = slot / K;", "const int64_t t = slot % K;"),
+    "softmax without the max shift": ("ex[e] = exp_cody_waite(row[e] - m);",
+                                      "ex[e] = exp_cody_waite(row[e]);"),
+    "softmax sum skips the first expert": ("      sum += ex[e];", "      if (e > 0) sum += ex[e];"),
+    "softmax max taken as the first logit": ("      if (row[e] > m) m = row[e];", "      (void)m;"),
     "permute copies the slot's row": ("out[p * H + h] = input[t * H + h];",
                                       "out[p * H + h] = input[(p / K) * H + h];"),
 }
@@ -93,6 +98,10 @@ def _pins():
         tsc.test_golden_fixture,
         tsg.test_error_bound_on_a_grid,
         tsg.test_special_values,
+        lambda: tsm.test_error_bound_against_float64(256),
+        tsm.test_large_logits_need_the_max_shift,
+        tsm.test_all_equal_row_is_exactly_uniform,
+        tsm.test_one_dominant_logit,
     ]
 
 
