@@ -371,6 +371,18 @@ def run_gpu(args, cfg, rank, world, local_rank):
         e[2].record(stream)
     torch.cuda.synchronize(dev)
     fused_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    # the single-launch variant (one cooperative kernel) on buffers of its own
+    single = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, dev, single_launch=True)
+    for i in range(ks):
+        flush_l2()
+        e = sev[i]
+        e[0].record(stream)
+        single.run(s_d, b_d, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    single_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    single_ok = single.device_status() == 0
+    del single
     status_ok = (moe.moe_read_device_status(pipe.fused_workspace) == 0
                  and moe.moe_read_device_status(pipe.index.workspace) == 0)
 
@@ -453,7 +465,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
     route_mean = statistics.fmean(route_ms)
     fin_gbs = nbytes["finalize"] / (fin_mean * 1e-3) / 1e9
     route_gbs = nbytes["route"] / (route_mean * 1e-3) / 1e9
-    launches_per_step = (1 if fused else 1 + index_launches(cfg.N, cfg.E)) + 1
+    launches_per_step = ((2 if cfg.N <= 1024 else 3) if fused
+                         else 1 + index_launches(cfg.N, cfg.E)) + 1
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -467,8 +480,9 @@ def run_gpu(args, cfg, rank, world, local_rank):
         "ms_per_step": worst_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded)",
-        "config": dict(config_dict(cfg), route_index="fused (moe_route_index, one launch)"
-                       if fused else "separate (moe_route, moe_create_indices)"),
+        "config": dict(config_dict(cfg), route_index="fused (moe_route_index: counting router, "
+                       "row prefixes, scatter)" if fused
+                       else "separate (moe_route, moe_create_indices)"),
         "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": fin_gbs, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": fin_gbs / peak,
                      "frac_vs_nominal_8tbs": fin_gbs / NOMINAL_HBM_GBS,
@@ -481,6 +495,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
                             "algorithmic_bytes_per_launch": nbytes["route"]},
         "stages_ms": {"route": route_mean, "create_indices": statistics.fmean(index_ms),
                       "route_index_fused": statistics.fmean(fused_ms),
+                      "route_index_single_launch": statistics.fmean(single_ms),
                       "finalize": statistics.fmean(fin_stage_ms),
                       "route_plus_index_in_timed_steps": statistics.fmean(
                           [e[0].elapsed_time(e[1]) for e in ev]),
@@ -518,7 +533,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "output_finite": out_ok,
-        "device_status_clean": status_ok,
+        "device_status_clean": status_ok and single_ok,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -16,7 +16,8 @@
  *   - Every pointer is a DEVICE pointer to a dense row-major buffer owned by
  *     the caller. The library allocates nothing, frees nothing and keeps no
  *     state between calls; the index builder's scratch space is a
- *     caller-provided workspace (moe_route_index keeps a call counter there).
+ *     caller-provided workspace (moe_route_index keeps counts there that every
+ *     call leaves at zero, moe_route_index_single_launch a call counter).
  *   - Every call only enqueues work on `stream` (0 = the legacy default
  *     stream) and returns without synchronising, except
  *     moe_read_device_status, which waits for the stream.
@@ -57,8 +58,8 @@ typedef enum {
 
 /* Bits of the device status word written by moe_create_indices and moe_route_index. */
 #define MOE_DEVICE_STATUS_BAD_EXPERT_ID 0x1u /* some topk_ids entry was outside [0, E) */
-#define MOE_DEVICE_STATUS_SYNC_TIMEOUT 0x2u  /* moe_route_index: a cross-CTA wait gave up */
-#define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* moe_route_index: inconsistent exchanged counts */
+#define MOE_DEVICE_STATUS_SYNC_TIMEOUT 0x2u  /* single-launch route+index: a cross-CTA wait gave up */
+#define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* single-launch route+index: inconsistent counts */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024       /* n_routed_experts / n_experts */
@@ -184,19 +185,23 @@ moe_status_t moe_create_indices(uint32_t* token_expert_order, uint32_t* expert_s
                                 cudaStream_t stream);
 
 /*
- * Workspace bytes that moe_route_index needs for num_tokens tokens and
- * n_routed_experts experts (always >= 2048). Host-only; returns 0 for
- * negative num_tokens or n_routed_experts outside [1, MOE_MAX_EXPERTS].
+ * Workspace bytes that moe_route_index needs for num_tokens tokens,
+ * n_routed_experts experts and n_experts_per_tok experts per token (always
+ * >= 4864). Host-only; returns 0 for negative num_tokens, n_routed_experts
+ * outside [1, MOE_MAX_EXPERTS] or n_experts_per_tok outside
+ * [1, MOE_MAX_EXPERTS_PER_TOK].
  */
-size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_experts);
+size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_experts,
+                                      int32_t n_experts_per_tok);
 
 /*
  * moe_route_index -- moe_route_ex followed by moe_create_indices on its
- * output, in one kernel launch.
+ * output, with the router counting its own output.
  * Pages "group_limited_router_kernel" (the routing: as moe_route and
  * moe_route_ex) and "moe_create_indices" (the index: as moe_create_indices
  * with topk_ids = expert_indices and num_slots = T*K). The pages launch the
- * two as separate kernels; fusing them is this library's design.
+ * two as separate kernels; fusing the count into the router is this
+ * library's design.
  *
  * Every output is bit-identical to those of the two separate calls:
  * expert_indices [T, K] int32 and expert_weights [T, K] fp32 (written, and
@@ -206,10 +211,56 @@ size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_exper
  * at moe_create_indices. Arguments and requirements are the union of
  * moe_route_ex's and moe_create_indices', plus T*K < 2^32 - 1.
  *
+ * Execution: the router adds each of its slots to a count per (expert,
+ * 1024-slot chunk) with a relaxed atomic (integer sums do not depend on the
+ * order, so the result is deterministic); a row-prefix kernel and the scatter
+ * kernel of moe_create_indices follow. Three launches in all (two when
+ * T*K <= 1024), no waits between CTAs.
  * workspace: device buffer of at least moe_route_index_workspace_size()
  *   bytes, 256-byte aligned, caller-owned, ZERO-FILLED before its first use
- *   (e.g. cudaMemset). Word 0 receives the device status word (read it with
- *   moe_read_device_status); word 1 counts the calls made on the workspace;
+ *   (e.g. cudaMemset): the router's counts accumulate into it, and every call
+ *   leaves them zero again, so the workspace is zeroed once, not per call.
+ *   The prefix matrix is placed at the end of workspace_bytes, so one
+ *   workspace may serve calls of any shapes that fit it, in any order.
+ *   Word 0 receives the device status word (moe_read_device_status). Calls
+ *   sharing one workspace must not overlap, and a workspace serves
+ *   moe_route_index or moe_route_index_single_launch, not both.
+ */
+moe_status_t moe_route_index(int32_t* expert_indices, float* expert_weights,
+                             uint32_t* token_expert_order, uint32_t* expert_start_indices,
+                             uint32_t* restore_token_order, int32_t* expert_ids,
+                             uint32_t* expert_usage_stats, const float* expert_scores,
+                             const float* expert_bias, int64_t num_tokens,
+                             int32_t n_routed_experts, int32_t n_experts_per_tok,
+                             int32_t n_groups, int32_t topk_group, int32_t norm_weights,
+                             float routed_scaling_factor, moe_score_fn_t score_fn,
+                             void* workspace, size_t workspace_bytes, uint32_t* scales_offset_p,
+                             cudaStream_t stream);
+
+/*
+ * Workspace bytes that moe_route_index_single_launch needs (always >= 2048).
+ * Host-only; returns 0 for negative num_tokens or n_routed_experts outside
+ * [1, MOE_MAX_EXPERTS].
+ */
+size_t moe_route_index_single_launch_workspace_size(int64_t num_tokens,
+                                                    int32_t n_routed_experts);
+
+/*
+ * moe_route_index_single_launch -- the same outputs as moe_route_index from
+ * ONE cooperative kernel launch.
+ * Every output is bit-identical to those of the two separate calls:
+ * expert_indices [T, K] int32 and expert_weights [T, K] fp32 (written, and
+ * also read back by the index build); token_expert_order [T*K],
+ * restore_token_order [T*K], expert_start_indices [E+1], expert_ids [E],
+ * expert_usage_stats [2] and the optional scales_offset_p [E+1] as described
+ * at moe_create_indices. Arguments and requirements are the union of
+ * moe_route_ex's and moe_create_indices', plus T*K < 2^32 - 1.
+ *
+ * workspace: device buffer of at least
+ *   moe_route_index_single_launch_workspace_size() bytes, 256-byte aligned,
+ *   caller-owned, ZERO-FILLED before its first use (e.g. cudaMemset). Word 0
+ *   receives the device status word (read it with moe_read_device_status);
+ *   word 1 counts the calls made on the workspace;
  *   the next 1024 bytes hold progress counters that each call zeroes for
  *   the next one.
  *   The CTAs of a call exchange their counts through words tagged with that
@@ -225,16 +276,14 @@ size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_exper
  * Returns MOE_ERR_UNSUPPORTED when the kernel cannot be made resident (no
  *   CTA fits on an SM), and MOE_ERR_CUDA when the cooperative launch fails.
  */
-moe_status_t moe_route_index(int32_t* expert_indices, float* expert_weights,
-                             uint32_t* token_expert_order, uint32_t* expert_start_indices,
-                             uint32_t* restore_token_order, int32_t* expert_ids,
-                             uint32_t* expert_usage_stats, const float* expert_scores,
-                             const float* expert_bias, int64_t num_tokens,
-                             int32_t n_routed_experts, int32_t n_experts_per_tok,
-                             int32_t n_groups, int32_t topk_group, int32_t norm_weights,
-                             float routed_scaling_factor, moe_score_fn_t score_fn,
-                             void* workspace, size_t workspace_bytes, uint32_t* scales_offset_p,
-                             cudaStream_t stream);
+moe_status_t moe_route_index_single_launch(
+    int32_t* expert_indices, float* expert_weights, uint32_t* token_expert_order,
+    uint32_t* expert_start_indices, uint32_t* restore_token_order, int32_t* expert_ids,
+    uint32_t* expert_usage_stats, const float* expert_scores, const float* expert_bias,
+    int64_t num_tokens, int32_t n_routed_experts, int32_t n_experts_per_tok, int32_t n_groups,
+    int32_t topk_group, int32_t norm_weights, float routed_scaling_factor,
+    moe_score_fn_t score_fn, void* workspace, size_t workspace_bytes, uint32_t* scales_offset_p,
+    cudaStream_t stream);
 
 /*
  * moe_finalize -- fused unpermute gather + top-k weighted row sum.

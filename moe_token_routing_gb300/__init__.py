@@ -11,14 +11,15 @@ from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_SYNC_STATE,
                       RouteIndexBuffers, create_indices, finalize, load_library,
                       moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
                       moe_finalize_ex, moe_permute, moe_read_device_status, moe_route,
-                      moe_route_ex, moe_route_index, moe_route_index_workspace_size, permute,
+                      moe_route_ex, moe_route_index, moe_route_index_single_launch_workspace_size,
+                      moe_route_index_workspace_size, permute,
                       route, route_index)
 from .pipeline import HostStreamer, RoutingPipeline
 
 __all__ = [
     "DEVICE_STATUS_BAD_EXPERT_ID", "DEVICE_STATUS_SYNC_STATE", "DEVICE_STATUS_SYNC_TIMEOUT",
     "EXPORTED_SYMBOLS", "RouteIndexBuffers", "moe_route_index", "moe_route_index_workspace_size",
-    "route_index", "HostStreamer", "IndexBuffers", "MoeError",
+    "moe_route_index_single_launch_workspace_size", "route_index", "HostStreamer", "IndexBuffers", "MoeError",
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
     "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
     "moe_finalize_ex", "moe_permute", "moe_read_device_status", "moe_route", "moe_route_ex",

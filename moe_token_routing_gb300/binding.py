@@ -29,7 +29,9 @@ DEVICE_STATUS_SYNC_STATE = 0x4
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
                     "moe_create_indices", "moe_finalize", "moe_read_device_status",
                     "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex",
-                    "moe_route_ex", "moe_route_index_workspace_size", "moe_route_index")
+                    "moe_route_ex", "moe_route_index_workspace_size", "moe_route_index",
+                    "moe_route_index_single_launch_workspace_size",
+                    "moe_route_index_single_launch")
 
 
 class MoeError(RuntimeError):
@@ -75,11 +77,14 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, ctypes.c_int,
                                  vp]
     lib.moe_route_ex.restype = ctypes.c_int
-    lib.moe_route_index_workspace_size.argtypes = [i64, i32]
+    lib.moe_route_index_workspace_size.argtypes = [i64, i32, i32]
     lib.moe_route_index_workspace_size.restype = sz
-    lib.moe_route_index.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
-                                    i32, f32, ctypes.c_int, vp, sz, vp, vp]
-    lib.moe_route_index.restype = ctypes.c_int
+    lib.moe_route_index_single_launch_workspace_size.argtypes = [i64, i32]
+    lib.moe_route_index_single_launch_workspace_size.restype = sz
+    for fn in (lib.moe_route_index, lib.moe_route_index_single_launch):
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32,
+                       ctypes.c_int, vp, sz, vp, vp]
+        fn.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -177,9 +182,15 @@ def moe_create_indices(token_expert_order: torch.Tensor, expert_start_indices: t
     _check("moe_create_indices", rc)
 
 
-def moe_route_index_workspace_size(num_tokens: int, n_routed_experts: int) -> int:
-    return int(load_library().moe_route_index_workspace_size(int(num_tokens),
-                                                             int(n_routed_experts)))
+def moe_route_index_workspace_size(num_tokens: int, n_routed_experts: int,
+                                   n_experts_per_tok: int) -> int:
+    return int(load_library().moe_route_index_workspace_size(
+        int(num_tokens), int(n_routed_experts), int(n_experts_per_tok)))
+
+
+def moe_route_index_single_launch_workspace_size(num_tokens: int, n_routed_experts: int) -> int:
+    return int(load_library().moe_route_index_single_launch_workspace_size(
+        int(num_tokens), int(n_routed_experts)))
 
 
 def moe_route_index(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
@@ -189,9 +200,10 @@ def moe_route_index(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
                     expert_bias: torch.Tensor, n_groups: int, topk_group: int,
                     norm_weights: bool, routed_scaling_factor: float, workspace: torch.Tensor,
                     score_fn: int = SCORES_AS_GIVEN, scales_offset: torch.Tensor | None = None,
-                    stream=None) -> None:
-    """Router and index build in one launch; the workspace must be zero-filled
-    before its first use (each call leaves its counters at zero)."""
+                    stream=None, single_launch: bool = False) -> None:
+    """Router and index build with the router counting its own output (or, with
+    single_launch, as one cooperative launch); the workspace must be
+    zero-filled before its first use and belongs to one of the two."""
     T, E = expert_scores.shape
     K = expert_indices.shape[1] if expert_indices.dim() == 2 else 0
     N = T * K
@@ -207,11 +219,12 @@ def moe_route_index(expert_indices: torch.Tensor, expert_weights: torch.Tensor,
     ws = _dev(workspace, "workspace", torch.uint8)
     so = None if scales_offset is None else _dev(scales_offset, "scales_offset", torch.int32,
                                                  (E + 1,))
-    rc = load_library().moe_route_index(*args, T, E, K, int(n_groups), int(topk_group),
-                                        int(bool(norm_weights)), float(routed_scaling_factor),
-                                        int(score_fn), ws, workspace.numel(), so,
-                                        _stream(stream))
-    _check("moe_route_index", rc)
+    lib = load_library()
+    fn = lib.moe_route_index_single_launch if single_launch else lib.moe_route_index
+    rc = fn(*args, T, E, K, int(n_groups), int(topk_group), int(bool(norm_weights)),
+            float(routed_scaling_factor), int(score_fn), ws, workspace.numel(), so,
+            _stream(stream))
+    _check("moe_route_index_single_launch" if single_launch else "moe_route_index", rc)
 
 
 def moe_finalize(output: torch.Tensor, down: torch.Tensor, restore_order: torch.Tensor,
@@ -336,11 +349,12 @@ class IndexBuffers:
 
 
 class RouteIndexBuffers:
-    """Preallocated outputs + zero-filled workspace of moe_route_index for T
-    tokens, E experts and K experts per token. The index outputs carry the
-    same names as IndexBuffers'."""
+    """Preallocated outputs + zero-filled workspace of moe_route_index (or of
+    moe_route_index_single_launch) for T tokens, E experts and K experts per
+    token. The index outputs carry the same names as IndexBuffers'."""
 
-    def __init__(self, T: int, E: int, K: int, device):
+    def __init__(self, T: int, E: int, K: int, device, single_launch: bool = False):
+        self.single_launch = bool(single_launch)
         self.T, self.E, self.K, self.N = T, E, K, T * K
         z = dict(dtype=torch.int32, device=device)
         self.expert_indices = torch.empty((T, K), **z)
@@ -350,7 +364,8 @@ class RouteIndexBuffers:
         self.restore_token_order = torch.empty(T * K, **z)
         self.expert_ids = torch.empty(E, **z)
         self.expert_usage_stats = torch.empty(2, **z)
-        ws = moe_route_index_workspace_size(T, E)
+        ws = (moe_route_index_single_launch_workspace_size(T, E) if self.single_launch
+              else moe_route_index_workspace_size(T, E, K))
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
 
     def run(self, expert_scores: torch.Tensor, expert_bias: torch.Tensor, n_groups: int,
@@ -361,7 +376,7 @@ class RouteIndexBuffers:
                         self.expert_start_indices, self.restore_token_order, self.expert_ids,
                         self.expert_usage_stats, expert_scores, expert_bias, n_groups,
                         topk_group, norm_weights, routed_scaling_factor, self.workspace,
-                        score_fn, scales_offset, stream)
+                        score_fn, scales_offset, stream, self.single_launch)
         return self
 
     def device_status(self, stream=None) -> int:
@@ -371,9 +386,9 @@ class RouteIndexBuffers:
 def route_index(expert_scores: torch.Tensor, expert_bias: torch.Tensor, n_experts_per_tok: int,
                 n_groups: int, topk_group: int, norm_weights: bool,
                 routed_scaling_factor: float, score_fn: int = SCORES_AS_GIVEN,
-                stream=None) -> RouteIndexBuffers:
+                stream=None, single_launch: bool = False) -> RouteIndexBuffers:
     T, E = expert_scores.shape
-    bufs = RouteIndexBuffers(T, E, n_experts_per_tok, expert_scores.device)
+    bufs = RouteIndexBuffers(T, E, n_experts_per_tok, expert_scores.device, single_launch)
     return bufs.run(expert_scores, expert_bias, n_groups, topk_group, norm_weights,
                     routed_scaling_factor, score_fn, stream=stream)
 

@@ -35,7 +35,6 @@ namespace {
 
 constexpr size_t kHeaderBytes = 256;
 constexpr int kCountThreads = kSlotsPerCta;  // one slot per thread in the count kernel
-constexpr int kRowsWarps = 8;                // rows kernel: warps per CTA, one expert each
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -90,144 +89,6 @@ __global__ void __launch_bounds__(kCountThreads) idx_count_kernel(const IdxArgs 
       a.counts[(int64_t)(j / pad) * a.row + a.num_blocks + j % pad] = 0u;
   }
   if (threadIdx.x == 0) a.flags[blockIdx.x] = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
-}
-
-// One warp per expert e: exclusive prefix of the row counts[e][0..row) in
-// place, 128 counts per pass (lane l takes counts 4l .. 4l+3 with one 16-byte
-// load), and the row total to totals[e]. The padding columns are zero.
-__global__ void __launch_bounds__(kRowsWarps * 32) idx_rows_kernel(const IdxArgs a) {
-  wait_for_prior_grid();
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRowsWarps + (threadIdx.x >> 5);
-  if (e >= a.E) return;
-  uint4* row = reinterpret_cast<uint4*>(a.counts + (int64_t)e * a.row);
-  const int Q = a.row / 4;
-  uint32_t carry = 0;
-  for (int q0 = 0; q0 < Q; q0 += 32) {
-    const int q = q0 + lane;
-    uint4 c = make_uint4(0u, 0u, 0u, 0u);
-    if (q < Q) c = row[q];
-    const uint32_t sum = c.x + c.y + c.z + c.w;
-    uint32_t incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
-    }
-    uint4 o;
-    o.x = carry + incl - sum;
-    o.y = o.x + c.x;
-    o.z = o.y + c.y;
-    o.w = o.z + c.z;
-    if (q < Q) row[q] = o;
-    carry += __shfl_sync(kFullMask, incl, 31);
-  }
-  if (lane == 0) a.totals[e] = carry;
-}
-
-// Where a scatter CTA takes its per-expert bases from.
-enum BaseSource : int {
-  kBasesSingleCta = 0,  // one CTA covers all slots: the bases are the expert starts
-  kBasesFromCounts = 1  // the last count CTA wrote them into the count matrix
-};
-
-template <int kBases>
-__global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs a) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* s_warp = smem;                      // [kIdxWarps][E]
-  uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
-  uint32_t* s_act = s_base + a.E;               // [E]
-  uint32_t* s_pad = s_act + a.E;                // [E]; then [E] totals, [E] prefixes
-  __shared__ uint32_t warp_tmp[32];
-  // With the count matrix from the count and rows kernels, this kernel is the
-  // third of the call, so the ids (written before the count kernel ran) are
-  // complete once it starts: the warp counts overlap the rows kernel's tail.
-  // A single CTA runs right after the ids' producer and must wait first.
-  if constexpr (kBases == kBasesSingleCta) wait_for_prior_grid();
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t* my_cnt = s_warp + warp * a.E;
-  for (int e = lane; e < a.E; e += 32) my_cnt[e] = 0;
-  __syncwarp();
-
-  const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
-  int v[kStepsPerWarp];
-  bool bad = false;
-  load_warp_slots(a, warp_base, v, bad);
-
-  // slots of each expert in this warp
-#pragma unroll
-  for (int s = 0; s < kStepsPerWarp; ++s) {
-    const unsigned peers = __match_any_sync(kFullMask, v[s]);
-    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
-    __syncwarp();
-  }
-  if constexpr (kBases == kBasesFromCounts) wait_for_prior_grid();  // counts, totals
-  __syncthreads();
-
-  if constexpr (kBases == kBasesSingleCta) {
-    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-      uint32_t t = 0;
-      for (int w = 0; w < kIdxWarps; ++w) t += s_warp[w * a.E + e];
-      s_base[e] = t;
-    }
-    __syncthreads();
-    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
-    const int any_bad = __syncthreads_or(bad);
-    if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
-  } else {
-    // totals -> expert starts, active and padded offsets in one pass; every
-    // CTA writes its share of the expert table and CTA 0 the status word;
-    // then base = start + this CTA's column of prefixes over earlier CTAs
-    __shared__ uint32_t s_flags;
-    const int b = blockIdx.x;
-    uint32_t* s_tot = s_pad + a.E;  // [E]
-    uint32_t* s_pre = s_tot + a.E;  // [E]
-    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-      s_tot[e] = a.totals[e];
-      s_pre[e] = a.counts[(int64_t)e * a.row + b];
-    }
-    if (threadIdx.x == 0) s_flags = 0;
-    __syncthreads();
-    const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
-    write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
-    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
-    if (b == 0) {
-      uint32_t f = 0;
-      for (int j = threadIdx.x; j < a.num_blocks; j += kIdxThreads) f |= a.flags[j];
-      f = __reduce_or_sync(kFullMask, f);
-      if (lane == 0 && f) atomicOr(&s_flags, f);
-      __syncthreads();
-      if (threadIdx.x == 0) *a.status = s_flags;
-    }
-  }
-  __syncthreads();
-  // per-warp running offsets: base + slots of e in earlier warps
-  for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-    uint32_t run = s_base[e];
-    for (int w = 0; w < kIdxWarps; ++w) {
-      const uint32_t c = s_warp[w * a.E + e];
-      s_warp[w * a.E + e] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
-
-  const unsigned lower = lanemask_lt();
-#pragma unroll
-  for (int s = 0; s < kStepsPerWarp; ++s) {
-    const int64_t i = warp_base + s * 32 + lane;
-    const unsigned peers = __match_any_sync(kFullMask, v[s]);
-    uint32_t pos = 0xFFFFFFFFu;
-    if (v[s] >= 0) pos = my_cnt[v[s]] + (uint32_t)__popc(peers & lower);
-    __syncwarp();
-    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
-    __syncwarp();
-    if (i < (int64_t)a.N) {
-      a.restore_token_order[i] = pos;
-      if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
-    }
-  }
 }
 
 moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream) {
@@ -287,7 +148,7 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
     return MOE_ERR_MISALIGNED;
 
   char* ws = static_cast<char*>(workspace);
-  IdxArgs a;
+  IdxArgs a{};
   a.ids = topk_ids;
   a.token_expert_order = token_expert_order;
   a.expert_start_indices = expert_start_indices;
@@ -295,10 +156,12 @@ extern "C" moe_status_t moe_create_indices(uint32_t* token_expert_order,
   a.expert_ids = expert_ids;
   a.stats = expert_usage_stats;
   a.scales_offset = scales_offset_p;
+  a.counts_from_router = 0;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.totals = reinterpret_cast<uint32_t*>(ws + L.totals_off);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
+  a.prefix = a.counts;  // prefixes in place of the counts
   a.N = (uint32_t)N;
   a.E = E;
   a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);
@@ -378,7 +241,7 @@ extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order
   // Every scratch word that a kernel reads is written earlier in the same
   // call, so nothing has to be cleared between calls.
   char* ws = static_cast<char*>(scratch);
-  IdxArgs a;
+  IdxArgs a{};
   a.ids = topk_ids;
   a.token_expert_order = token_expert_order;
   a.expert_start_indices = expert_start_indices;
@@ -386,10 +249,12 @@ extern "C" moe_status_t moe_create_indices_no_alloc(uint32_t* token_expert_order
   a.expert_ids = expert_ids;
   a.stats = expert_usage_stats;
   a.scales_offset = nullptr;
+  a.counts_from_router = 0;
   a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(ws);
   a.totals = reinterpret_cast<uint32_t*>(ws + L.totals_off);
   a.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   a.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
+  a.prefix = a.counts;  // prefixes in place of the counts
   a.N = (uint32_t)N;
   a.E = E;
   a.num_blocks = (int)(L.num_blocks > 0 ? L.num_blocks : 1);

@@ -221,7 +221,7 @@ extern "C" moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
                                      int64_t num_tokens, int32_t num_experts_per_token,
                                      int64_t hidden, cudaStream_t stream) {
   using namespace moe;
-  FinArgs a;
+  FinArgs a{};
   const moe_status_t st = check_and_pack(output, 2, down, restore_order, router_weight, 4,
                                          num_tokens, num_experts_per_token, hidden, &a);
   if (st != MOE_OK || num_tokens == 0 || hidden == 0) return st;
@@ -237,7 +237,7 @@ extern "C" moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype,
   const bool out_f32 = output_dtype == MOE_DTYPE_F32, w_f32 = weight_dtype == MOE_DTYPE_F32;
   if ((output_dtype != MOE_DTYPE_BF16 && !out_f32) || (weight_dtype != MOE_DTYPE_BF16 && !w_f32))
     return MOE_ERR_UNSUPPORTED;
-  FinArgs a;
+  FinArgs a{};
   const moe_status_t st = check_and_pack(output, out_f32 ? 4 : 2, down, restore_order,
                                          router_weight, w_f32 ? 4 : 2, num_tokens,
                                          num_experts_per_token, hidden, &a);

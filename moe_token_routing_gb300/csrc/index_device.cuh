@@ -14,8 +14,8 @@ constexpr int kIdxWarps = kIdxThreads / 32;
 constexpr int kStepsPerWarp = 4;
 constexpr int kSlotsPerWarp = 32 * kStepsPerWarp;
 constexpr int kSlotsPerCta = kIdxWarps * kSlotsPerWarp;  // 1024
-constexpr int kScanThreads = 1024;
 constexpr uint32_t kScaleRowAlign = MOE_SCALES_ROW_ALIGNMENT;
+constexpr int kRowsWarps = 8;  // rows kernel: warps per CTA, one expert each
 
 struct IdxArgs {
   const int32_t* ids;
@@ -26,9 +26,11 @@ struct IdxArgs {
   uint32_t* stats;
   uint32_t* status;  // workspace word 0
   uint32_t* flags;   // [num_blocks]
-  uint32_t* counts;  // [E][row]; the rows kernel turns each row into prefixes
+  uint32_t* counts;  // [E][row] counts of each expert in each CTA chunk
+  uint32_t* prefix;  // [E][row]: the rows kernel's prefixes (may be `counts` itself)
   uint32_t* totals;  // [E]: slots of each expert
   uint32_t* scales_offset;  // optional [E+1]: 128-row aligned per-expert offsets
+  int counts_from_router;   // counts accumulated by the router (see idx_rows_kernel)
   uint32_t N;
   int E;
   int num_blocks;
@@ -247,6 +249,163 @@ __device__ __forceinline__ void load_warp_slots(const IdxArgs& a, int64_t warp_b
     v[s] = id;
   }
 }
+
+// ---------------------------------------------------------------- kernels shared by
+// moe_create_indices and moe_route_index
+
+// Where a scatter CTA takes its per-expert bases from.
+enum BaseSource : int {
+  kBasesSingleCta = 0,  // one CTA covers all slots: the bases are the expert starts
+  kBasesFromCounts = 1  // the rows kernel turned the count matrix into prefixes
+};
+
+// One warp per expert e: exclusive prefix of the row counts[e][0..row) into
+// prefix[e][..] (in place when they are the same array), 128 counts per pass
+// (lane l takes counts 4l .. 4l+3 with one 16-byte load), and the row total to
+// totals[e]. The padding columns are zero. With counts from the router the
+// row is left zero for the next call's atomics, in the same coalesced pass.
+__global__ void __launch_bounds__(kRowsWarps * 32) idx_rows_kernel(const IdxArgs a) {
+  wait_for_prior_grid();
+  // counts from the router: no count kernel wrote flags, so the status word
+  // starts here and the scatter CTAs add their bits to it
+  if (a.counts_from_router && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRowsWarps + (threadIdx.x >> 5);
+  if (e >= a.E) return;
+  uint4* row = reinterpret_cast<uint4*>(a.counts + (int64_t)e * a.row);
+  uint4* out = reinterpret_cast<uint4*>(a.prefix + (int64_t)e * a.row);
+  const int Q = a.row / 4;
+  uint32_t carry = 0;
+  for (int q0 = 0; q0 < Q; q0 += 32) {
+    const int q = q0 + lane;
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);
+    if (q < Q) c = row[q];
+    const uint32_t sum = c.x + c.y + c.z + c.w;
+    uint32_t incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += y;
+    }
+    uint4 o;
+    o.x = carry + incl - sum;
+    o.y = o.x + c.x;
+    o.z = o.y + c.y;
+    o.w = o.z + c.z;
+    if (q < Q) {
+      out[q] = o;
+      if (a.counts_from_router) row[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    carry += __shfl_sync(kFullMask, incl, 31);
+  }
+  if (lane == 0) a.totals[e] = carry;
+}
+
+
+template <int kBases>
+__global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs a) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* s_warp = smem;                      // [kIdxWarps][E]
+  uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
+  uint32_t* s_act = s_base + a.E;               // [E]
+  uint32_t* s_pad = s_act + a.E;                // [E]; then [E] totals, [E] prefixes
+  __shared__ uint32_t warp_tmp[32];
+  // With the count matrix from the count and rows kernels, this kernel is the
+  // third of the call, so the ids (written before the count kernel ran) are
+  // complete once it starts: the warp counts overlap the rows kernel's tail.
+  // A single CTA runs right after the ids' producer and must wait first.
+  if constexpr (kBases == kBasesSingleCta) wait_for_prior_grid();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* my_cnt = s_warp + warp * a.E;
+  for (int e = lane; e < a.E; e += 32) my_cnt[e] = 0;
+  __syncwarp();
+
+  const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
+  int v[kStepsPerWarp];
+  bool bad = false;
+  load_warp_slots(a, warp_base, v, bad);
+
+  // slots of each expert in this warp
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
+    __syncwarp();
+  }
+  if constexpr (kBases == kBasesFromCounts) wait_for_prior_grid();  // counts, totals
+  __syncthreads();
+
+  if constexpr (kBases == kBasesSingleCta) {
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+      uint32_t t = 0;
+      for (int w = 0; w < kIdxWarps; ++w) t += s_warp[w * a.E + e];
+      s_base[e] = t;
+    }
+    __syncthreads();
+    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
+  } else {
+    // totals -> expert starts, active and padded offsets in one pass; every
+    // CTA writes its share of the expert table and CTA 0 the status word;
+    // then base = start + this CTA's column of prefixes over earlier CTAs
+    __shared__ uint32_t s_flags;
+    const int b = blockIdx.x;
+    uint32_t* s_tot = s_pad + a.E;  // [E]
+    uint32_t* s_pre = s_tot + a.E;  // [E]
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+      s_tot[e] = a.totals[e];
+      s_pre[e] = a.prefix[(int64_t)e * a.row + b];
+    }
+    if (threadIdx.x == 0) s_flags = 0;
+    __syncthreads();
+    const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
+    write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
+    __syncthreads();  // the table share reads starts that other threads update next
+    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
+    if (b == 0 && !a.counts_from_router) {
+      uint32_t f = 0;
+      for (int j = threadIdx.x; j < a.num_blocks; j += kIdxThreads) f |= a.flags[j];
+      f = __reduce_or_sync(kFullMask, f);
+      if (lane == 0 && f) atomicOr(&s_flags, f);
+      __syncthreads();
+      if (threadIdx.x == 0) *a.status = s_flags;
+    }
+  }
+  __syncthreads();
+  // per-warp running offsets: base + slots of e in earlier warps
+  for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
+    uint32_t run = s_base[e];
+    for (int w = 0; w < kIdxWarps; ++w) {
+      const uint32_t c = s_warp[w * a.E + e];
+      s_warp[w * a.E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+
+  const unsigned lower = lanemask_lt();
+#pragma unroll
+  for (int s = 0; s < kStepsPerWarp; ++s) {
+    const int64_t i = warp_base + s * 32 + lane;
+    const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    uint32_t pos = 0xFFFFFFFFu;
+    if (v[s] >= 0) pos = my_cnt[v[s]] + (uint32_t)__popc(peers & lower);
+    __syncwarp();
+    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
+    __syncwarp();
+    if (i < (int64_t)a.N) {
+      a.restore_token_order[i] = pos;
+      if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
+    }
+  }
+  if constexpr (kBases == kBasesFromCounts) {
+    if (a.counts_from_router && __syncthreads_or(bad) && threadIdx.x == 0)
+      atomicOr(a.status, MOE_DEVICE_STATUS_BAD_EXPERT_ID);
+  }
+}
+
 
 }  // namespace
 }  // namespace moe

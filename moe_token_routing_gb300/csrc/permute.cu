@@ -118,7 +118,7 @@ extern "C" moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* inpu
   const uintptr_t i0 = (uintptr_t)input, i1 = i0 + (uintptr_t)(T * hidden * 2);
   if (o0 < i1 && i0 < o1) return MOE_ERR_INVALID_ARG;
 
-  PermArgs a;
+  PermArgs a{};
   a.out = reinterpret_cast<uint4*>(permuted);
   a.in = reinterpret_cast<const uint4*>(input);
   a.restore = restore_token_order;

@@ -492,15 +492,189 @@ moe_status_t launch_fused_thread(const RoutePlan& p, const FusedArgs& f, cudaStr
   return launch_fused(route_index_thread_kernel<EP, false>, f, W, 32 * W, smem, stream);
 }
 
+// ---------------------------------------------------------------- three-kernel path
+// moe_route_index: the router counts its own output, so the index build starts
+// at the row prefixes. Slot i = t*K+k of expert e adds one to counts[e][i /
+// 1024] (a relaxed atomic: integer sums do not depend on the order); the
+// rows kernel turns each expert's row into prefixes and totals; the scatter
+// CTA of chunk b places its 1024 slots and leaves column b zero again for the
+// next call. No CTA waits on another: the kernel boundaries order the phases.
+
+struct CountRouteArgs {
+  RouteArgs r;
+  uint32_t* counts;  // [E][row], zero on entry; nullptr: route without counting
+  int row;
+};
+
+__device__ __forceinline__ void count_slot(const CountRouteArgs& c, int64_t slot, int id) {
+  if (c.counts != nullptr && (unsigned)id < (unsigned)c.r.E)
+    atomicAdd(c.counts + (int64_t)id * c.row + slot / kSlotsPerCta, 1u);
+}
+
+template <int C, bool kVec, bool kSoftmax>
+__global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2)
+    route_count_warp_kernel(const CountRouteArgs c) {
+  extern __shared__ float dyn_smem[];  // kRouteWarps * c.r.warp_smem_words
+  wait_for_prior_grid();
+  const int warp = threadIdx.x >> 5;
+  const int64_t K = c.r.K;
+  route_tokens_warp<C, kVec, kSoftmax>(
+      c.r, (int64_t)blockIdx.x * kRouteWarps + warp, c.r.T, (int64_t)gridDim.x * kRouteWarps,
+      dyn_smem + warp * c.r.warp_smem_words,
+      [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
+}
+
+template <int EP, bool kVec>
+__global__ void __launch_bounds__(kRouteThreads) route_count_thread_kernel(const CountRouteArgs c) {
+  wait_for_prior_grid();
+  const int64_t K = c.r.K;
+  route_tokens_thread<EP, kVec>(c.r, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, c.r.T,
+                                (int64_t)gridDim.x * blockDim.x,
+                                [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
+}
+
+// Workspace of the three-kernel path: header (word 0: status) | totals
+// [MOE_MAX_EXPERTS] | counts [E][row] ... prefixes [E][row] at the END of the
+// caller's workspace. Every call leaves its counts zero, the counts start at a
+// fixed place and the prefixes end at the workspace's end; since each call's
+// counts and prefixes both fit, no call's counts reach words that another
+// call's prefixes left nonzero, whatever the shapes and their order.
+struct SplitLayout {
+  int64_t num_blocks, row;
+  size_t totals_off, counts_off, matrix_bytes, total;
+};
+
+SplitLayout split_layout(int64_t N, int E) {
+  SplitLayout L;
+  L.num_blocks = (N + kSlotsPerCta - 1) / kSlotsPerCta;
+  if (L.num_blocks < 1) L.num_blocks = 1;
+  L.row = (L.num_blocks + 3) & ~(int64_t)3;
+  L.totals_off = kFusedHeaderBytes;
+  L.counts_off = L.totals_off + sizeof(uint32_t) * MOE_MAX_EXPERTS;
+  L.matrix_bytes = round256(sizeof(uint32_t) * (size_t)E * (size_t)L.row);
+  L.total = L.counts_off + 2 * L.matrix_bytes;
+  return L;
+}
+
+template <typename Kernel, typename Args>
+moe_status_t launch_counting_router(Kernel k, const Args& args, int64_t T, int64_t tokens_per_cta,
+                                    size_t smem, cudaStream_t stream) {
+  if (smem > 40 * 1024 &&
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kRouteThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (T + tokens_per_cta - 1) / tokens_per_cta;
+  const int64_t cap = (int64_t)device_info().sm_count * per_sm;
+  const int grid = (int)(want < cap ? want : cap);
+  return launch(k, grid, kRouteThreads, smem, stream, args);
+}
+
+template <int C, bool kSoftmax>
+moe_status_t launch_count_warp_fn(const RoutePlan& p, const CountRouteArgs& c,
+                                  cudaStream_t stream) {
+  const size_t smem = route_warp_smem(p, kRouteWarps);
+  if constexpr (C % 4 == 0) {
+    if (p.vec)
+      return launch_counting_router(route_count_warp_kernel<C, true, kSoftmax>, c, c.r.T,
+                                    kRouteWarps, smem, stream);
+  }
+  return launch_counting_router(route_count_warp_kernel<C, false, kSoftmax>, c, c.r.T,
+                                kRouteWarps, smem, stream);
+}
+
+template <int C>
+moe_status_t launch_count_warp(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_count_warp_fn<C, true>(p, c, stream);
+  return launch_count_warp_fn<C, false>(p, c, stream);
+}
+
+template <int EP>
+moe_status_t launch_count_thread(const RoutePlan& p, const CountRouteArgs& c,
+                                 cudaStream_t stream) {
+  if (p.vec)
+    return launch_counting_router(route_count_thread_kernel<EP, true>, c, c.r.T, kRouteThreads,
+                                  0, stream);
+  return launch_counting_router(route_count_thread_kernel<EP, false>, c, c.r.T, kRouteThreads, 0,
+                                stream);
+}
+
+moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
+                                   cudaStream_t stream) {
+  switch (p.C) {
+    case 0:
+      if (p.EP == 8) return launch_count_thread<8>(p, c, stream);
+      if (p.EP == 16) return launch_count_thread<16>(p, c, stream);
+      return launch_count_thread<32>(p, c, stream);
+    case 2: return launch_count_warp<2>(p, c, stream);
+    case 4: return launch_count_warp<4>(p, c, stream);
+    case 8: return launch_count_warp<8>(p, c, stream);
+    case 16: return launch_count_warp<16>(p, c, stream);
+    default: return launch_count_warp<32>(p, c, stream);
+  }
+}
+
+// The rows and scatter kernels (index_device.cuh) after the counting router.
+moe_status_t launch_rows_scatter(const IdxArgs& a, cudaStream_t stream) {
+  const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * a.E;
+  if (scatter_smem > 40 * 1024 &&
+      cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromCounts>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)scatter_smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const moe_status_t st = launch(idx_rows_kernel, (a.E + kRowsWarps - 1) / kRowsWarps,
+                                 kRowsWarps * 32, 0, stream, a);
+  if (st != MOE_OK) return st;
+  return launch(idx_scatter_kernel<kBasesFromCounts>, a.num_blocks, kIdxThreads, scatter_smem,
+                stream, a);
+}
+
+// Checks shared by both entry points; fills the router plan.
+moe_status_t check_route_index(int32_t* expert_indices, float* expert_weights,
+                               uint32_t* token_expert_order, uint32_t* expert_start_indices,
+                               uint32_t* restore_token_order, int32_t* expert_ids,
+                               uint32_t* expert_usage_stats, const float* expert_scores,
+                               const float* expert_bias, int64_t num_tokens,
+                               int32_t n_routed_experts, int32_t n_experts_per_tok,
+                               int32_t n_groups, int32_t topk_group, int32_t norm_weights,
+                               float routed_scaling_factor, int32_t score_fn,
+                               uint32_t* scales_offset_p, RoutePlan* p) {
+  moe_status_t st = plan_route(expert_indices, expert_weights, expert_scores, expert_bias,
+                               num_tokens, n_routed_experts, n_experts_per_tok, n_groups,
+                               topk_group, norm_weights, routed_scaling_factor, score_fn, p);
+  if (st != MOE_OK) return st;
+  const int64_t T = num_tokens, E = n_routed_experts;
+  const int64_t N = T * n_experts_per_tok;
+  if (N > (int64_t)0xFFFFFFFEu) return MOE_ERR_UNSUPPORTED;
+  if (scales_offset_p != nullptr && N + (int64_t)(kScaleRowAlign - 1) * E > (int64_t)0xFFFFFFFFu)
+    return MOE_ERR_UNSUPPORTED;
+  if (!expert_start_indices || !expert_ids || !expert_usage_stats) return MOE_ERR_NULL_PTR;
+  if (T > 0) {
+    st = check_route_pointers(p->a);
+    if (st != MOE_OK) return st;
+    if (!token_expert_order || !restore_token_order) return MOE_ERR_NULL_PTR;
+  }
+  if (!aligned(token_expert_order, 4) || !aligned(expert_start_indices, 4) ||
+      !aligned(restore_token_order, 4) || !aligned(expert_ids, 4) ||
+      !aligned(expert_usage_stats, 4) || !aligned(scales_offset_p, 4))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
-extern "C" size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_experts) {
+extern "C" size_t moe_route_index_single_launch_workspace_size(int64_t num_tokens,
+                                                                int32_t n_routed_experts) {
   if (num_tokens < 0 || n_routed_experts < 1 || n_routed_experts > MOE_MAX_EXPERTS) return 0;
   return moe::fused_layout(num_tokens, n_routed_experts).total;
 }
 
-extern "C" moe_status_t moe_route_index(
+extern "C" moe_status_t moe_route_index_single_launch(
     int32_t* expert_indices, float* expert_weights, uint32_t* token_expert_order,
     uint32_t* expert_start_indices, uint32_t* restore_token_order, int32_t* expert_ids,
     uint32_t* expert_usage_stats, const float* expert_scores, const float* expert_bias,
@@ -510,32 +684,21 @@ extern "C" moe_status_t moe_route_index(
     cudaStream_t stream) {
   using namespace moe;
   RoutePlan p;
-  moe_status_t st = plan_route(expert_indices, expert_weights, expert_scores, expert_bias,
-                               num_tokens, n_routed_experts, n_experts_per_tok, n_groups,
-                               topk_group, norm_weights, routed_scaling_factor, score_fn, &p);
+  moe_status_t st = check_route_index(
+      expert_indices, expert_weights, token_expert_order, expert_start_indices,
+      restore_token_order, expert_ids, expert_usage_stats, expert_scores, expert_bias, num_tokens,
+      n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights,
+      routed_scaling_factor, score_fn, scales_offset_p, &p);
   if (st != MOE_OK) return st;
   const int64_t T = num_tokens, E = n_routed_experts;
   const int64_t N = T * n_experts_per_tok;
-  if (N > (int64_t)0xFFFFFFFEu) return MOE_ERR_UNSUPPORTED;
-  if (scales_offset_p != nullptr && N + (int64_t)(kScaleRowAlign - 1) * E > (int64_t)0xFFFFFFFFu)
-    return MOE_ERR_UNSUPPORTED;
-  if (!expert_start_indices || !expert_ids || !expert_usage_stats) return MOE_ERR_NULL_PTR;
-  if (T > 0) {
-    st = check_route_pointers(p.a);
-    if (st != MOE_OK) return st;
-    if (!token_expert_order || !restore_token_order) return MOE_ERR_NULL_PTR;
-  }
   const FusedLayout L = fused_layout(T, (int)E);
   if (!workspace || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
-  if (!aligned(token_expert_order, 4) || !aligned(expert_start_indices, 4) ||
-      !aligned(restore_token_order, 4) || !aligned(expert_ids, 4) ||
-      !aligned(expert_usage_stats, 4) || !aligned(scales_offset_p, 4))
-    return MOE_ERR_MISALIGNED;
 
   char* ws = static_cast<char*>(workspace);
   uint32_t* header = reinterpret_cast<uint32_t*>(ws);
-  FusedArgs f;
+  FusedArgs f{};
   f.r = p.a;
   f.x.ids = expert_indices;
   f.x.token_expert_order = token_expert_order;
@@ -547,6 +710,8 @@ extern "C" moe_status_t moe_route_index(
   f.x.flags = nullptr;
   f.x.counts = nullptr;
   f.x.totals = nullptr;
+  f.x.prefix = nullptr;
+  f.x.counts_from_router = 0;
   f.x.scales_offset = scales_offset_p;
   f.x.N = (uint32_t)N;
   f.x.E = (int)E;
@@ -571,4 +736,72 @@ extern "C" moe_status_t moe_route_index(
     case 16: return launch_fused_warp<16>(p, f, stream);
     default: return launch_fused_warp<32>(p, f, stream);
   }
+}
+
+extern "C" size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_experts,
+                                                 int32_t n_experts_per_tok) {
+  if (num_tokens < 0 || n_routed_experts < 1 || n_routed_experts > MOE_MAX_EXPERTS ||
+      n_experts_per_tok < 1 || n_experts_per_tok > MOE_MAX_EXPERTS_PER_TOK)
+    return 0;
+  return moe::split_layout(num_tokens * n_experts_per_tok, n_routed_experts).total;
+}
+
+extern "C" moe_status_t moe_route_index(
+    int32_t* expert_indices, float* expert_weights, uint32_t* token_expert_order,
+    uint32_t* expert_start_indices, uint32_t* restore_token_order, int32_t* expert_ids,
+    uint32_t* expert_usage_stats, const float* expert_scores, const float* expert_bias,
+    int64_t num_tokens, int32_t n_routed_experts, int32_t n_experts_per_tok, int32_t n_groups,
+    int32_t topk_group, int32_t norm_weights, float routed_scaling_factor,
+    moe_score_fn_t score_fn, void* workspace, size_t workspace_bytes, uint32_t* scales_offset_p,
+    cudaStream_t stream) {
+  using namespace moe;
+  RoutePlan p;
+  moe_status_t st = check_route_index(
+      expert_indices, expert_weights, token_expert_order, expert_start_indices,
+      restore_token_order, expert_ids, expert_usage_stats, expert_scores, expert_bias, num_tokens,
+      n_routed_experts, n_experts_per_tok, n_groups, topk_group, norm_weights,
+      routed_scaling_factor, score_fn, scales_offset_p, &p);
+  if (st != MOE_OK) return st;
+  const int64_t T = num_tokens, N = T * n_experts_per_tok;
+  const SplitLayout L = split_layout(N, n_routed_experts);
+  if (!workspace || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
+
+  char* ws = static_cast<char*>(workspace);
+  IdxArgs x{};
+  x.ids = expert_indices;
+  x.token_expert_order = token_expert_order;
+  x.expert_start_indices = expert_start_indices;
+  x.restore_token_order = restore_token_order;
+  x.expert_ids = expert_ids;
+  x.stats = expert_usage_stats;
+  x.status = reinterpret_cast<uint32_t*>(ws);
+  x.flags = nullptr;
+  x.counts = reinterpret_cast<uint32_t*>(ws + L.counts_off);
+  x.totals = reinterpret_cast<uint32_t*>(ws + L.totals_off);
+  // prefixes at the end of the caller's workspace, 256-byte aligned
+  x.prefix = reinterpret_cast<uint32_t*>(ws + (workspace_bytes - L.matrix_bytes) / 256 * 256);
+  x.scales_offset = scales_offset_p;
+  x.counts_from_router = 1;
+  x.N = (uint32_t)N;
+  x.E = n_routed_experts;
+  x.num_blocks = (int)L.num_blocks;
+  x.row = (int)L.row;
+
+  CountRouteArgs c{};
+  c.r = p.a;
+  c.counts = L.num_blocks > 1 ? x.counts : nullptr;
+  c.row = (int)L.row;
+  if (T > 0) {
+    st = launch_counting_route(p, c, stream);
+    if (st != MOE_OK) return st;
+  }
+  if (L.num_blocks > 1) return launch_rows_scatter(x, stream);
+  // one CTA places every slot (and writes the status word) without counts
+  const size_t smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * x.E;
+  if (smem > 40 * 1024 &&
+      cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launch(idx_scatter_kernel<kBasesSingleCta>, 1, kIdxThreads, smem, stream, x);
 }

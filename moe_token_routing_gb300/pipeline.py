@@ -36,7 +36,7 @@ class RoutingPipeline:
         self.index = IndexBuffers(T * K, E, self.device)
         self.fused_workspace = None
         if self.fused:
-            self.fused_workspace = torch.zeros(moe_route_index_workspace_size(T, E),
+            self.fused_workspace = torch.zeros(moe_route_index_workspace_size(T, E, K),
                                                dtype=torch.uint8, device=self.device)
         self.output = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
         self._staged = None

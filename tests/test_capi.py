@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
         ["moe_status_string", "moe_route", "moe_create_indices_workspace_size",
          "moe_create_indices", "moe_finalize", "moe_read_device_status",
          "moe_create_indices_no_alloc", "moe_permute", "moe_finalize_ex", "moe_route_ex",
-         "moe_route_index_workspace_size", "moe_route_index"])
+         "moe_route_index_workspace_size", "moe_route_index",
+         "moe_route_index_single_launch_workspace_size", "moe_route_index_single_launch"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -59,7 +60,27 @@ def test_workspace_size_query(lib):
     assert lib.moe_create_indices_workspace_size(10, 1025) == 0
 
 
-def route_index_workspace_bytes(T, E):
+def route_index_workspace_bytes(T, E, K):
+    """256-byte header, a fixed [1024] block of per-expert totals, then room
+    for the [E][row] count and prefix matrices (row = the 1024-slot chunks
+    rounded up to 4), each rounded up to 256 bytes."""
+    chunks = max(-(-(T * K) // 1024), 1)
+    row = (chunks + 3) // 4 * 4
+    return 256 + 4 * 1024 + 2 * ((4 * E * row + 255) // 256 * 256)
+
+
+def test_route_index_workspace_size_query(lib):
+    f = lib.moe_route_index_workspace_size
+    for T, E, K in ((0, 8, 2), (64, 256, 8), (16384, 256, 8), (131072, 8, 2), (33, 96, 5)):
+        assert f(T, E, K) == route_index_workspace_bytes(T, E, K), (T, E, K)
+    assert f(0, 8, 1) == 4352 + 512
+    assert f(-1, 8, 2) == 0
+    assert f(10, 0, 2) == 0
+    assert f(10, 8, 0) == 0
+    assert f(10, 8, 33) == 0
+
+
+def single_launch_workspace_bytes(T, E):
     """256-byte header, four 256-byte counter blocks, then [E][R] tagged counts
     and prefixes, E tagged totals
     and R tagged status words (8 bytes each), every part rounded up to 256
@@ -70,10 +91,10 @@ def route_index_workspace_bytes(T, E):
     return 256 + 1024 + 2 * r256(8 * E * R) + r256(8 * E) + r256(8 * R)
 
 
-def test_route_index_workspace_size_query(lib):
-    f = lib.moe_route_index_workspace_size
+def test_single_launch_workspace_size_query(lib):
+    f = lib.moe_route_index_single_launch_workspace_size
     for T, E in ((0, 8), (64, 256), (16384, 256), (131072, 8), (10 ** 9, 1024), (33, 96)):
-        assert f(T, E) == route_index_workspace_bytes(T, E), (T, E)
+        assert f(T, E) == single_launch_workspace_bytes(T, E), (T, E)
     assert f(0, 8) == 2304
     assert f(16384, 256) == 256 + 1024 + 2 * 8 * 256 * 2048 + 2048 + 8 * 2048
     assert f(-1, 8) == 0
@@ -124,11 +145,13 @@ def test_create_indices_host_validation(lib):
     assert f(FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE, 10, 64, FAKE, ws, None, None) == 3
 
 
-def test_route_index_host_validation(lib):
-    f = lib.moe_route_index
+@pytest.mark.parametrize("single", [False, True])
+def test_route_index_host_validation(lib, single):
+    f = lib.moe_route_index_single_launch if single else lib.moe_route_index
     outs = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
     ins = (FAKE, FAKE)
-    ws = lib.moe_route_index_workspace_size(1000, 256)
+    ws = (lib.moe_route_index_single_launch_workspace_size(1000, 256) if single
+          else lib.moe_route_index_workspace_size(1000, 256, 8))
     cfg = (1000, 256, 8, 8, 4, 1, 1.0)
     assert f(*outs, *ins, *cfg, 7, FAKE, ws, None, None) == 4          # unknown score loader
     assert f(*outs, *ins, 1000, 256, 8, 7, 4, 1, 1.0, 0, FAKE, ws, None, None) == 2  # E % G

@@ -1,7 +1,7 @@
-"""GPU parity of moe_route_index: the group-limited router (page
-"group_limited_router_kernel") and the index build (page "moe_create_indices")
-in one cooperative launch, against the oracle's route followed by its
-create_indices.
+"""GPU parity of moe_route_index and moe_route_index_single_launch: the
+group-limited router (page "group_limited_router_kernel") and the index build
+(page "moe_create_indices"), with the router counting its own output or in one
+cooperative launch, against the oracle's route followed by its create_indices.
 
 Ids and every index output are bit-exact; the weights are the router's fp32
 arithmetic and are compared bit for bit as well (the same device code makes
@@ -29,13 +29,14 @@ def _moe():
     return moe
 
 
-def gpu_route_index(scores, bias, K, G, M, norm, scale, score_fn=0, scales=False, bufs=None):
+def gpu_route_index(scores, bias, K, G, M, norm, scale, score_fn=0, scales=False, bufs=None,
+                    single=False):
     moe = _moe()
     s = torch.from_numpy(np.ascontiguousarray(scores)).cuda()
     b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
     T, E = scores.shape
     if bufs is None:
-        bufs = moe.RouteIndexBuffers(T, E, K, "cuda")
+        bufs = moe.RouteIndexBuffers(T, E, K, "cuda", single_launch=single)
     so = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda") if scales else None
     bufs.run(s, b, G, M, norm, scale, score_fn, scales_offset=so)
     torch.cuda.synchronize()
@@ -67,10 +68,15 @@ def check(scores, bias, K, G, M, norm, scale, **kw):
     return got, bufs, ids_ref
 
 
+BOTH = pytest.mark.parametrize("single", [False, True], ids=["counting", "single_launch"])
+
+
+@BOTH
 @pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
-def test_parity_on_workloads(name):
+def test_parity_on_workloads(name, single):
     cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
-    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                                single=single)
     assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
     assert bufs.device_status() == 0
 
@@ -83,37 +89,42 @@ SHAPES = [(8, 1, 1, 2), (8, 4, 2, 3), (12, 3, 2, 4), (16, 4, 2, 4), (32, 4, 2, 8
           (1024, 32, 4, 8)]
 
 
+@BOTH
 @pytest.mark.parametrize("E,G,M,K", SHAPES)
 @pytest.mark.parametrize("T", [1, 333, 5000])
-def test_parity_shapes(E, G, M, K, T):
+def test_parity_shapes(E, G, M, K, T, single):
     rng = np.random.default_rng(E * 7919 + G * 31 + M * 7 + K + T)
     scores = rng.random((T, E), dtype=np.float32)
     bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
-    check(scores, bias, K, G, M, True, 1.5)
+    check(scores, bias, K, G, M, True, 1.5, single=single)
 
 
-@pytest.mark.parametrize("T", [0, 1, 7, 8, 9, 255, 257, 4097, 100003])
-def test_token_counts_prefill_shape(T):
+@BOTH
+@pytest.mark.parametrize("T", [0, 1, 7, 8, 9, 128, 129, 255, 257, 4097, 100003])
+def test_token_counts_prefill_shape(T, single):
     cfg = synth.get_config("dsv3_prefill")
     scores = synth.make_scores(cfg, n_tokens=T) if T else np.zeros((0, cfg.E), np.float32)
     bias = synth.make_bias(cfg)
-    got, _, _ = check(scores, bias, cfg.K, cfg.G, cfg.M, True, 2.5)
+    got, _, _ = check(scores, bias, cfg.K, cfg.G, cfg.M, True, 2.5, single=single)
     if T == 0:
         assert (got["expert_ids"] == -1).all() and (got["expert_start_indices"] == 0).all()
         assert got["expert_usage_stats"].tolist() == [0, 0]
 
 
+@BOTH
 @pytest.mark.parametrize("E,G,M,K,T", [(8, 1, 1, 2, 2_000_000), (64, 8, 4, 8, 200_000)])
-def test_several_placement_rounds_per_cta(E, G, M, K, T):
-    """Many more slots per warp than one placement round holds, so each warp
-    places its slots in several rounds (thread path and warp path)."""
+def test_large_token_counts(E, G, M, K, T, single):
+    """Large batches: for the single launch, many more slots per warp than one
+    placement round holds; for the counting path, count rows longer than one
+    pass of the row-prefix kernel (thread path and warp path)."""
     rng = np.random.default_rng(T)
     scores = rng.random((T, E), dtype=np.float32)
     bias = np.zeros(E, np.float32)
-    check(scores, bias, K, G, M, False, 1.0)
+    check(scores, bias, K, G, M, False, 1.0, single=single)
 
 
-def test_hot_experts_and_ties():
+@BOTH
+def test_hot_experts_and_ties(single):
     """Scores on a 1/8 grid plus a large bias on four experts: many equal keys
     and a few experts holding most slots."""
     rng = np.random.default_rng(5)
@@ -121,12 +132,13 @@ def test_hot_experts_and_ties():
     scores = (rng.integers(0, 9, size=(T, E)) / 8).astype(np.float32)
     bias = np.zeros(E, np.float32)
     bias[[3, 17, 64, 100]] = 2.0
-    got, _, _ = check(scores, bias, 8, 8, 4, True, 1.0)
+    got, _, _ = check(scores, bias, 8, 8, 4, True, 1.0, single=single)
     assert got["expert_usage_stats"][0] >= T // 2
 
 
+@BOTH
 @pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_prefill", "few_expert_large_batch"])
-def test_sigmoid_loader(name):
+def test_sigmoid_loader(name, single):
     cfg = synth.get_config(name)
     logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
     bias = synth.make_bias(cfg)
@@ -135,40 +147,64 @@ def test_sigmoid_loader(name):
     idx_ref = oracle.create_indices(ids_ref, cfg.E)
     moe = _moe()
     got, _ = gpu_route_index(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
-                             score_fn=moe.SCORES_SIGMOID)
+                             score_fn=moe.SCORES_SIGMOID, single=single)
     assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
 
 
+@BOTH
 @pytest.mark.parametrize("name", ["tiny", "dsv3_prefill", "skewed_ungrouped"])
-def test_scales_offsets(name):
+def test_scales_offsets(name, single):
     cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
     got, _ = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
-                             scales=True)
+                             scales=True, single=single)
     assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
     assert np.array_equal(got["scales"], oracle.scales_offsets(ids_ref, cfg.E))
 
 
+def test_counts_left_zero_and_calls_repeat():
+    """The counting path leaves its whole count matrix zero after each call
+    (the prefixes live elsewhere, at the workspace's end), so repeated calls on
+    one workspace need no clearing."""
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("dsv3_prefill")
+    bufs = None
+    for _ in range(3):
+        got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
+                                    cfg.scale, bufs=bufs)
+        assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+        # header (256 B) | totals (1024 words) | counts [E][row] | ... prefixes at the end
+        row = (-(-cfg.T * cfg.K // 1024) + 3) // 4 * 4
+        matrix = -(-4 * cfg.E * row // 256) * 256
+        counts = bufs.workspace[256 + 4 * 1024:256 + 4 * 1024 + matrix].view(torch.int32)
+        assert int(counts.abs().sum().item()) == 0
+        assert bufs.device_status() == 0
+
+
 def test_call_counter_advances_and_calls_repeat():
-    """Header word 1 counts the calls; nothing is cleared between calls."""
+    """Single launch: header word 1 counts the calls; nothing is cleared
+    between calls."""
     cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("dsv3_prefill")
     bufs = None
     for n in range(1, 4):
         got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
-                                    cfg.scale, bufs=bufs)
+                                    cfg.scale, bufs=bufs, single=True)
         assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
         header = bufs.workspace[:8].view(torch.int32).cpu().numpy()
         assert header.tolist() == [0, n]
 
 
-def test_workspace_reused_across_shapes():
-    """Words left tagged by a larger call never pass for a smaller call's."""
+@BOTH
+def test_workspace_reused_across_shapes(single):
+    """One workspace, sized for the largest call, serves calls of other shapes
+    in any order: stale tagged words never pass for a later call's (single
+    launch), and the count matrix of any layout starts zero (counting)."""
     moe = _moe()
     big = synth.get_config("dsv3_prefill")
-    ws = torch.zeros(moe.moe_route_index_workspace_size(big.T, big.E), dtype=torch.uint8,
-                     device="cuda")
-    for name in ("dsv3_prefill", "dsv3_decode", "tiny", "dsv3_prefill"):
+    nbytes = (moe.moe_route_index_single_launch_workspace_size(big.T, big.E) if single
+              else moe.moe_route_index_workspace_size(big.T, big.E, big.K))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for name in ("dsv3_prefill", "dsv3_decode", "tiny", "skewed_ungrouped", "dsv3_prefill"):
         cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
-        bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda")
+        bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda", single_launch=single)
         bufs.workspace = ws
         got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
                                     cfg.scale, bufs=bufs)
@@ -180,7 +216,7 @@ def test_call_counter_wraps_past_zero():
     """Call number 0 is skipped, so a zero-filled word never looks current."""
     moe = _moe()
     cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("skewed_ungrouped")
-    bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda")
+    bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda", single_launch=True)
     bufs.workspace[:8].view(torch.int32)[1] = -1
     got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
                                 bufs=bufs)
@@ -251,8 +287,9 @@ def test_fused_pipeline_matches_separate_launches():
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
 
 
+@BOTH
 @pytest.mark.parametrize("name", ["dsv3_decode", "skewed_ungrouped", "few_expert_large_batch"])
-def test_softmax_loader(name):
+def test_softmax_loader(name, single):
     cfg = synth.get_config(name)
     logits = synth.normal_f32(cfg.seed, synth.TENSOR_SCORES, cfg.T * cfg.E).reshape(cfg.T, cfg.E)
     bias = synth.make_bias(cfg)
@@ -261,5 +298,5 @@ def test_softmax_loader(name):
     idx_ref = oracle.create_indices(ids_ref, cfg.E)
     moe = _moe()
     got, _ = gpu_route_index(logits, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
-                             score_fn=moe.SCORES_SOFTMAX)
+                             score_fn=moe.SCORES_SOFTMAX, single=single)
     assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
