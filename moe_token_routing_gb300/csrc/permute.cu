@@ -86,12 +86,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const PermArgs a)
 
 template <int K>
 moe_status_t launch_permute(const PermArgs& a, cudaStream_t stream) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_kernel<K>, kPermThreads, 0) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const int64_t cap = (int64_t)device_info().sm_count * per_sm;
+  // one CTA per token, as in finalize: tokens go to SMs as CTAs retire
+  const int64_t cap = 0x7fffffff;
   const int grid = (int)(a.T < cap ? a.T : cap);
   return launch(permute_kernel<K>, grid, kPermThreads, 0, stream, a);
 }

@@ -6,8 +6,12 @@
 // selection only (Args expert_bias, expert_weights); Parameters norm_weights
 // and Args routed_scaling_factor fix the weight post-processing.
 //
-// Two kernel shapes:
-//  * E > 32: one warp per token. Lane l holds the C = E/32 (rounded up to a
+// Three kernel shapes:
+//  * E = 32*L (L = 2 .. 32, a power of two), K <= 8, groups of whole lanes: L
+//    lanes per token, 32 experts per lane; sorting networks over 32-bit
+//    selection keys that carry the expert in their low bits, with the warp
+//    path below as the exact fallback for near-equal scores (route_tokens_seg).
+//  * other E > 32: one warp per token. Lane l holds the C = E/32 (rounded up to a
 //    power of two) contiguous experts l*C .. l*C+C-1 in registers. Group
 //    scores come from a per-lane top-2 plus a butterfly over the lanes of a
 //    group; the expert top-K is K rounds of a warp-wide max (redux.sync on
@@ -32,6 +36,17 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
                              [](int64_t, int, int) {});
 }
 
+template <int L, bool kGroups>
+__global__ void __launch_bounds__(kRouteThreads, 4) route_seg_kernel(const RouteArgs a) {
+  __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
+  wait_for_prior_grid();
+  if (threadIdx.x < 32) stage_seg_bias(a, s_bias);
+  __syncthreads();
+  const int warps = blockDim.x >> 5;
+  route_tokens_seg<L, kGroups>(a, s_bias, (int64_t)blockIdx.x * warps + (threadIdx.x >> 5),
+                               (int64_t)gridDim.x * warps, [](int64_t, int, int) {});
+}
+
 template <int EP, bool kVec>
 __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const RouteArgs a) {
   wait_for_prior_grid();
@@ -40,26 +55,21 @@ __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const Route
 }
 
 template <typename Kernel>
-int ctas_per_sm(Kernel k, size_t smem) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRouteThreads, smem) != cudaSuccess ||
-      n < 1)
-    n = 1;
-  return n;
-}
-
-template <typename Kernel>
 moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, size_t smem,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int threads = kRouteThreads) {
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
   }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
   const int64_t want = (a.T + tokens_per_cta - 1) / tokens_per_cta;
-  const int64_t cap = (int64_t)device_info().sm_count * ctas_per_sm(k, smem);
+  const int64_t cap = (int64_t)device_info().sm_count * per_sm;
   const int grid = (int)(want < cap ? want : cap);
-  return launch(k, grid, kRouteThreads, smem, stream, a);
+  return launch(k, grid, threads, smem, stream, a);
 }
 
 template <int C, bool kSoftmax>
@@ -76,6 +86,15 @@ template <int C>
 moe_status_t launch_warp_path(const RoutePlan& p, cudaStream_t stream) {
   if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_warp_path_fn<C, true>(p, stream);
   return launch_warp_path_fn<C, false>(p, stream);
+}
+
+template <int L>
+moe_status_t launch_seg_path(const RoutePlan& p, cudaStream_t stream) {
+  const int warps = seg_warps_per_cta(p.a.T, L, device_info().sm_count);
+  const int64_t tokens_per_cta = (int64_t)warps * (32 / L);
+  if (p.a.group_mode == kGroupsAllKept)
+    return launch_route(route_seg_kernel<L, false>, p.a, tokens_per_cta, 0, stream, 32 * warps);
+  return launch_route(route_seg_kernel<L, true>, p.a, tokens_per_cta, 0, stream, 32 * warps);
 }
 
 template <int EP>
@@ -97,6 +116,14 @@ moe_status_t route_impl(int32_t* expert_indices, float* expert_weights,
   if (num_tokens == 0) return MOE_OK;
   st = check_route_pointers(p.a);
   if (st != MOE_OK) return st;
+  switch (p.seg) {
+    case 2: return launch_seg_path<2>(p, stream);
+    case 4: return launch_seg_path<4>(p, stream);
+    case 8: return launch_seg_path<8>(p, stream);
+    case 16: return launch_seg_path<16>(p, stream);
+    case 32: return launch_seg_path<32>(p, stream);
+    default: break;
+  }
   switch (p.C) {
     case 0:
       if (p.EP == 8) return launch_thread_path<8>(p, stream);

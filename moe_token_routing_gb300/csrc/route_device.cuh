@@ -42,6 +42,11 @@ struct RouteArgs {
   // layout's biased scores, then E for the token's softmax scores.
   int warp_smem_words;
   int softmax_off;
+  // Segment layout: an expert's selection key keeps the top 32 - key_bits
+  // bits of its order key and carries key_low - e in the low key_bits bits
+  // (key_low = 2^key_bits - 1, key_bits = bits of E - 1).
+  int key_bits;
+  uint32_t key_low;
 };
 
 // exp(x) in fp32 by Cody-Waite range reduction (W. J. Cody and W. Waite,
@@ -374,6 +379,296 @@ __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t fi
 }
 
 
+// ---------------------------------------------------------------- segment layout
+// E = 32*L experts (L = 2 .. 32, a power of two), K <= 8: a segment of L lanes
+// routes one token, so a warp routes 32/L tokens at once; lane j of a segment
+// holds experts 32j .. 32j+31. Every expert gets a 32-bit selection key: the
+// order key of its biased score with the low key_bits bits replaced by key_low
+// - e. The keys are unique and name their expert, and two keys whose order
+// keys differ above bit key_bits compare as (score desc, expert asc). Each
+// lane sorts its 32 keys into a top-8 with sorting networks of unsigned
+// min/max, the segment merges its lanes' lists in log2(L) butterfly steps,
+// and the first K of the merged list are the token's experts. This equals the
+// exact selection whenever the first K+1 keys differ above bit key_bits: then
+// every other candidate's order key is below all K chosen ones and the chosen
+// ones keep their order. Otherwise (two near-equal scores at the top, about
+// 0.4% of the tokens of the prefill workload) the token is routed again by the
+// exact warp path.
+
+constexpr int kSegKeys = 32;        // experts per lane
+constexpr int kSegTop = 8;          // length of the sorted lists (K <= 8)
+constexpr int kSegBiasStride = 36;  // shared-memory floats per lane block of bias
+
+__device__ __forceinline__ void cmpx_desc(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b);
+  b = min(a, b);
+  a = hi;
+}
+
+// Sorts 8 keys into descending order (Batcher's odd-even merge sort: 19
+// comparators in 6 layers).
+__device__ __forceinline__ void sort8_desc(uint32_t (&x)[8]) {
+  cmpx_desc(x[0], x[1]); cmpx_desc(x[2], x[3]); cmpx_desc(x[4], x[5]); cmpx_desc(x[6], x[7]);
+  cmpx_desc(x[0], x[2]); cmpx_desc(x[1], x[3]); cmpx_desc(x[4], x[6]); cmpx_desc(x[5], x[7]);
+  cmpx_desc(x[1], x[2]); cmpx_desc(x[5], x[6]);
+  cmpx_desc(x[0], x[4]); cmpx_desc(x[1], x[5]); cmpx_desc(x[2], x[6]); cmpx_desc(x[3], x[7]);
+  cmpx_desc(x[2], x[4]); cmpx_desc(x[3], x[5]);
+  cmpx_desc(x[1], x[2]); cmpx_desc(x[3], x[4]); cmpx_desc(x[5], x[6]);
+}
+
+// a := the 8 largest keys of the descending lists a and b, descending. The
+// element-wise maximum of a and reversed b holds exactly those keys and is
+// bitonic, so three half-cleaner layers sort it (K. E. Batcher, "Sorting
+// networks and their applications", 1968).
+__device__ __forceinline__ void merge8_desc(uint32_t (&a)[8], const uint32_t (&b)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = max(a[i], b[7 - i]);
+  cmpx_desc(a[0], a[4]); cmpx_desc(a[1], a[5]); cmpx_desc(a[2], a[6]); cmpx_desc(a[3], a[7]);
+  cmpx_desc(a[0], a[2]); cmpx_desc(a[1], a[3]); cmpx_desc(a[4], a[6]); cmpx_desc(a[5], a[7]);
+  cmpx_desc(a[0], a[1]); cmpx_desc(a[2], a[3]); cmpx_desc(a[4], a[5]); cmpx_desc(a[6], a[7]);
+}
+
+// x[i] for a run-time i in [0, 8) without local memory.
+__device__ __forceinline__ uint32_t pick8(const uint32_t (&x)[8], int i) {
+  uint32_t r = x[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) r = (i == q) ? x[q] : r;
+  return r;
+}
+
+// Selection key of a biased score b that is not -0 (the staged bias holds no
+// -0, and x + y is -0 only when both are -0), so the order key needs no
+// zero fold.
+__device__ __forceinline__ uint32_t selection_key(const RouteArgs& a, float b, uint32_t tag) {
+  const uint32_t u = __float_as_uint(b);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return (k & ~a.key_low) | tag;
+}
+
+// Biased scores of this lane's 32 experts of row t (score function applied).
+__device__ __forceinline__ void load_seg_scores(const RouteArgs& a, const float* row,
+                                                const float* bias_j, float (&b)[kSegKeys]) {
+#pragma unroll
+  for (int q = 0; q < kSegKeys / 4; ++q) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
+    b[4 * q + 0] = v.x;
+    b[4 * q + 1] = v.y;
+    b[4 * q + 2] = v.z;
+    b[4 * q + 3] = v.w;
+  }
+  if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+#pragma unroll
+    for (int i = 0; i < kSegKeys; ++i) b[i] = apply_score_fn(a.score_fn, b[i]);
+  }
+#pragma unroll
+  for (int q = 0; q < kSegKeys / 4; ++q) {
+    const float4 c = *reinterpret_cast<const float4*>(bias_j + 4 * q);
+    b[4 * q + 0] = __fadd_rn(b[4 * q + 0], c.x);
+    b[4 * q + 1] = __fadd_rn(b[4 * q + 1], c.y);
+    b[4 * q + 2] = __fadd_rn(b[4 * q + 2], c.z);
+    b[4 * q + 3] = __fadd_rn(b[4 * q + 3], c.w);
+  }
+}
+
+// Copies the bias into shared memory in the segment layout (call from warp
+// 0, then __syncthreads): lane block j at s_bias + kSegBiasStride * j, so
+// the eight 16-byte loads of a quarter warp hit distinct banks. A -0 bias is
+// stored as +0: s + (-0) and s + (+0) differ only for s = -0, where they give
+// -0 and +0, which compare equal, so no selection or group score changes and
+// no biased score is ever -0. The loads are independent 16-byte loads (E is a
+// multiple of 32 and the plan requires a 16-byte aligned bias).
+__device__ __forceinline__ void stage_seg_bias(const RouteArgs& a, float* s_bias) {
+  const int lane = threadIdx.x & 31;
+  const float4* src = reinterpret_cast<const float4*>(a.bias);
+  float4 v[MOE_MAX_EXPERTS / 128];
+#pragma unroll
+  for (int q = 0; q < MOE_MAX_EXPERTS / 128; ++q) {
+    const int i = lane + 32 * q;  // float4 index: experts 4i .. 4i+3
+    if (4 * i < a.E) v[q] = __ldg(src + i);
+  }
+#pragma unroll
+  for (int q = 0; q < MOE_MAX_EXPERTS / 128; ++q) {
+    const int i = lane + 32 * q;
+    if (4 * i < a.E) {
+      const int e = 4 * i;
+      const float4 f = make_float4(__fadd_rn(v[q].x, 0.0f), __fadd_rn(v[q].y, 0.0f),
+                                   __fadd_rn(v[q].z, 0.0f), __fadd_rn(v[q].w, 0.0f));
+      *reinterpret_cast<float4*>(s_bias + kSegBiasStride * (e / kSegKeys) + e % kSegKeys) = f;
+    }
+  }
+}
+
+// The exact warp path for one token, out of line: it runs for few tokens, and
+// keeping it out of the segment loop keeps that loop's code small.
+template <int L, typename OnId>
+__device__ __noinline__ void route_one_token_exact(const RouteArgs a, int64_t t, OnId on_id) {
+  // (the warp path's vector loads need C = L to be a multiple of 4)
+  route_tokens_warp<L, L % 4 == 0, false>(a, t, t + 1, 1, nullptr, on_id);
+}
+
+// Warps per CTA of a segment-layout launch: 8, or fewer when 8-warp CTAs
+// would leave SMs without one (few tokens per warp-iteration count: 32/L
+// tokens each).
+inline int seg_warps_per_cta(int64_t T, int L, int sm_count) {
+  const int64_t iters = (T + 32 / L - 1) / (32 / L);
+  if (iters >= (int64_t)sm_count * kRouteWarps) return kRouteWarps;
+  const int64_t w = (iters + 4 * (int64_t)sm_count - 1) / (4 * (int64_t)sm_count);
+  return (int)(w < 1 ? 1 : w);
+}
+
+// Routes the tokens of warps warp_id, warp_id + num_warps, ... (32/L tokens
+// each) with the calling warp; s_bias is the bias from stage_seg_bias. After
+// token t's ids and weights are written, on_id(t, k, id) is called once per
+// k < K. kGroups: topk_group < n_groups (a group spans L/G whole lanes).
+template <int L, bool kGroups, typename OnId>
+__device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float* s_bias,
+                                                 int64_t warp_id, int64_t num_warps,
+                                                 OnId on_id) {
+  static_assert(L >= 2 && L <= 32 && (L & (L - 1)) == 0, "segments of 2 .. 32 lanes");
+  constexpr int kTokens = 32 / L;                 // tokens per warp
+  constexpr int kOut = (kSegTop + L - 1) / L;     // list entries a lane writes out
+  const int lane = threadIdx.x & 31;
+  const int j = lane & (L - 1);
+  const int seg_base = lane & ~(L - 1);
+  const int e0 = kSegKeys * j;
+  const uint32_t tag0 = a.key_low - (uint32_t)e0;
+  const int gl = kGroups ? L / a.G : L;  // lanes per group
+  const int grp = j / gl;
+  const float* bias_j = s_bias + kSegBiasStride * j;
+
+  for (int64_t base = warp_id * kTokens; base < a.T; base += num_warps * kTokens) {
+    const int64_t t = base + lane / L;
+    const bool live = t < a.T;
+    const float* row = a.scores + (live ? t : base) * a.E;
+
+    // ---- selection keys, the group's top-2 and this lane's sorted top-8 ----
+    uint32_t key[4][8];
+    float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+    {
+      float b[kSegKeys];
+      load_seg_scores(a, row + e0, bias_j, b);
+#pragma unroll
+      for (int i = 0; i < kSegKeys; ++i) {
+        key[i / 8][i % 8] = selection_key(a, b[i], tag0 - (uint32_t)i);
+        if constexpr (kGroups) top2_push(t1, t2, b[i]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sort8_desc(key[q]);
+    merge8_desc(key[0], key[1]);
+    merge8_desc(key[2], key[3]);
+    merge8_desc(key[0], key[2]);
+    uint32_t (&mine)[8] = key[0];
+
+    // ---- group selection: the group's top-2 sum ranked against the others ----
+    if constexpr (kGroups) {
+      for (int off = 1; off < gl; off <<= 1) {
+        const float o1 = __shfl_xor_sync(kFullMask, t1, off);
+        const float o2 = __shfl_xor_sync(kFullMask, t2, off);
+        t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+        t1 = fmaxf(t1, o1);
+      }
+      const float g = __fadd_rn(t1, t2);
+      int ahead = 0;
+#pragma unroll
+      for (int h = 0; h < L; ++h) {  // groups h < G (G <= L)
+        const float og = __shfl_sync(kFullMask, g, seg_base + (h * gl & (L - 1)));
+        ahead += h < a.G && ((og > g) || (og == g && h < grp));
+      }
+      if (ahead >= a.M) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mine[i] = 0u;
+      }
+    }
+
+    // ---- the segment's top-8 ----
+    uint32_t top[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) top[i] = mine[i];
+#pragma unroll
+    for (int off = 1; off < L; off <<= 1) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(kFullMask, top[i], off);
+      merge8_desc(top, o);
+    }
+
+    // ---- the (K+1)-th key: in the list, or the best key below it ----
+    uint32_t next;
+    if (a.K < kSegTop) {
+      next = pick8(top, a.K);
+    } else {
+      const uint32_t last = top[7];
+      int taken = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) taken += mine[i] >= last;
+      next = taken < 8 ? pick8(mine, taken) : 0u;
+      if (taken == 8 && last != 0u) {
+        // all eight of this lane's listed keys were chosen: its next key is
+        // the best of the other 24, recomputed from the scores
+        float b[kSegKeys];
+        load_seg_scores(a, row + e0, bias_j, b);
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) {
+          const uint32_t k = selection_key(a, b[i], tag0 - (uint32_t)i);
+          next = k < last ? max(next, k) : next;
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < L; off <<= 1) next = max(next, __shfl_xor_sync(kFullMask, next, off));
+    }
+
+    // ---- exact unless two of the first K+1 keys agree above bit key_bits ----
+    bool redo = pick8(top, a.K - 1) == 0u;
+#pragma unroll
+    for (int r = 0; r < kSegTop; ++r) {
+      if (r < a.K) {
+        const uint32_t nx = r + 1 < a.K ? top[r + 1 < 8 ? r + 1 : 7] : next;
+        redo = redo || ((top[r] ^ nx) >> a.key_bits) == 0u;
+      }
+    }
+
+    // ---- ids and weights (list entries j, j + L, ...) ----
+    const bool write = live && !redo;
+    int id[kOut];
+    float w[kOut];
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) {
+      const int k = j + L * o;
+      id[o] = (int)(a.key_low - (pick8(top, k) & a.key_low));
+      w[o] = 0.0f;
+      if (write && k < a.K) w[o] = apply_score_fn(a.score_fn, __ldg(row + id[o]));
+    }
+    if (a.norm) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kSegTop; ++k)
+        if (k < a.K) sum = __fadd_rn(sum, __shfl_sync(kFullMask, w[k / L], seg_base + k % L));
+#pragma unroll
+      for (int o = 0; o < kOut; ++o) w[o] = __fdiv_rn(w[o], sum);
+    }
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) {
+      const int k = j + L * o;
+      if (write && k < a.K) {
+        a.ids[t * a.K + k] = id[o];
+        a.weights[t * a.K + k] = __fmul_rn(w[o], a.scale);
+        on_id(t, k, id[o]);
+      }
+    }
+
+    // ---- tokens whose top keys tied: the exact warp path, one token at a time ----
+    unsigned pending = __ballot_sync(kFullMask, live && redo && j == 0);
+    while (pending) {
+      const int l0 = __ffs(pending) - 1;
+      pending &= pending - 1;
+      const int64_t tr = base + l0 / L;
+      route_one_token_exact<L>(a, tr, on_id);
+    }
+  }
+}
+
+
 // Routes tokens first, first + stride, ... (below end) with the calling
 // thread, all E <= EP <= 32 scores in registers. After token t's ids and
 // weights are written, on_id(t, k, id) is called for k = 0 .. K-1.
@@ -506,6 +801,7 @@ struct RoutePlan {
   int C;    // warp path (E > 32): experts per lane; 0 selects the thread path
   int EP;   // thread path: E rounded up to 8, 16 or 32
   bool vec; // 16-byte score loads (E % 4 == 0 and a 16-byte aligned score matrix)
+  int seg;  // segment layout: lanes per token (E = 32 * seg); 0 when it does not apply
 };
 
 // Checks the router's sizes and options and fills `p` (pointers are taken as
@@ -545,6 +841,10 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   a.score_fn = score_fn;
   a.warp_smem_words = 0;
   a.softmax_off = 0;
+  a.key_bits = 1;
+  while ((1 << a.key_bits) < E) ++a.key_bits;
+  a.key_low = (1u << a.key_bits) - 1u;
+  p->seg = 0;
   p->vec = (E % 4 == 0) && aligned(expert_scores, 16);
   p->C = 0;
   p->EP = E <= 8 ? 8 : E <= 16 ? 16 : 32;
@@ -561,6 +861,14 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   }
   a.softmax_off = a.group_mode == kGroupsGeneric ? E : 0;
   a.warp_smem_words = a.softmax_off + (score_fn == MOE_SCORES_SOFTMAX ? E : 0);
+  // the segment layout: E a power-of-two multiple of 32, K <= 8, 16-byte
+  // loads, groups of whole lanes; the warp path with C = E / 32 is its exact
+  // fallback
+  const int L = E / kSegKeys;
+  if (E == kSegKeys * p->C && K <= kSegTop && p->vec && aligned(expert_bias, 16) &&
+      score_fn != MOE_SCORES_SOFTMAX &&
+      (a.group_mode == kGroupsAllKept || (a.group_mode == kGroupsSegment && G <= L && L % G == 0)))
+    p->seg = L;
   return MOE_OK;
 }
 

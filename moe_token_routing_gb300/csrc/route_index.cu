@@ -524,6 +524,19 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2)
       [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
 }
 
+template <int L, bool kGroups>
+__global__ void __launch_bounds__(kRouteThreads, 4) route_count_seg_kernel(const CountRouteArgs c) {
+  __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
+  wait_for_prior_grid();
+  if (threadIdx.x < 32) stage_seg_bias(c.r, s_bias);
+  __syncthreads();
+  const int warps = blockDim.x >> 5;
+  const int64_t K = c.r.K;
+  route_tokens_seg<L, kGroups>(c.r, s_bias, (int64_t)blockIdx.x * warps + (threadIdx.x >> 5),
+                               (int64_t)gridDim.x * warps,
+                               [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
+}
+
 template <int EP, bool kVec>
 __global__ void __launch_bounds__(kRouteThreads) route_count_thread_kernel(const CountRouteArgs c) {
   wait_for_prior_grid();
@@ -558,20 +571,20 @@ SplitLayout split_layout(int64_t N, int E) {
 
 template <typename Kernel, typename Args>
 moe_status_t launch_counting_router(Kernel k, const Args& args, int64_t T, int64_t tokens_per_cta,
-                                    size_t smem, cudaStream_t stream) {
+                                    size_t smem, cudaStream_t stream,
+                                    int threads = kRouteThreads) {
   if (smem > 40 * 1024 &&
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return MOE_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kRouteThreads, smem) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const int64_t want = (T + tokens_per_cta - 1) / tokens_per_cta;
   const int64_t cap = (int64_t)device_info().sm_count * per_sm;
   const int grid = (int)(want < cap ? want : cap);
-  return launch(k, grid, kRouteThreads, smem, stream, args);
+  return launch(k, grid, threads, smem, stream, args);
 }
 
 template <int C, bool kSoftmax>
@@ -603,8 +616,27 @@ moe_status_t launch_count_thread(const RoutePlan& p, const CountRouteArgs& c,
                                 stream);
 }
 
+template <int L>
+moe_status_t launch_count_seg(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
+  const int warps = seg_warps_per_cta(c.r.T, L, device_info().sm_count);
+  const int64_t tokens_per_cta = (int64_t)warps * (32 / L);
+  if (p.a.group_mode == kGroupsAllKept)
+    return launch_counting_router(route_count_seg_kernel<L, false>, c, c.r.T, tokens_per_cta, 0,
+                                  stream, 32 * warps);
+  return launch_counting_router(route_count_seg_kernel<L, true>, c, c.r.T, tokens_per_cta, 0,
+                                stream, 32 * warps);
+}
+
 moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
                                    cudaStream_t stream) {
+  switch (p.seg) {
+    case 2: return launch_count_seg<2>(p, c, stream);
+    case 4: return launch_count_seg<4>(p, c, stream);
+    case 8: return launch_count_seg<8>(p, c, stream);
+    case 16: return launch_count_seg<16>(p, c, stream);
+    case 32: return launch_count_seg<32>(p, c, stream);
+    default: break;
+  }
   switch (p.C) {
     case 0:
       if (p.EP == 8) return launch_count_thread<8>(p, c, stream);

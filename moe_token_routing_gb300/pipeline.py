@@ -20,12 +20,14 @@ from .binding import (IndexBuffers, moe_finalize, moe_permute, moe_read_device_s
 
 
 class RoutingPipeline:
-    """``fused=True`` runs route and create_indices as one launch
-    (moe_route_index); the outputs are the same bits either way."""
+    """``fused=True`` (the default) builds the indices with moe_route_index,
+    whose router counts its own output, so route and create_indices take three
+    launches instead of four; ``fused=False`` calls moe_route and then
+    moe_create_indices. The outputs are the same bits either way."""
 
     def __init__(self, T: int, E: int, K: int, H: int, n_groups: int, topk_group: int,
                  norm_weights: bool, routed_scaling_factor: float, device="cuda",
-                 fused: bool = False):
+                 fused: bool = True):
         self.T, self.E, self.K, self.H = T, E, K, H
         self.n_groups, self.topk_group = n_groups, topk_group
         self.norm_weights, self.scale = bool(norm_weights), float(routed_scaling_factor)
@@ -49,7 +51,7 @@ class RoutingPipeline:
         self.index.run(self.expert_indices, stream)
 
     def route_index(self, expert_scores, expert_bias, stream=None):
-        """route + create_indices in one launch (needs ``fused=True``)."""
+        """route + create_indices through moe_route_index (needs ``fused=True``)."""
         if self.fused_workspace is None:
             raise RuntimeError("RoutingPipeline was built with fused=False")
         ix = self.index

@@ -11,17 +11,18 @@ from _workloads import (bits_to_f32, f32_to_bf16_bits, finalize_tolerance_ok, wo
 pytestmark = pytest.mark.gpu
 
 
-def _pipe(cfg):
+def _pipe(cfg, fused=True):
     import moe_token_routing_gb300 as moe
     return moe.RoutingPipeline(cfg.T, cfg.E, cfg.K, cfg.H, cfg.G, cfg.M, cfg.norm_weights,
-                               cfg.scale, device="cuda")
+                               cfg.scale, device="cuda", fused=fused)
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["route_index", "separate"])
 @pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
-def test_chain_matches_oracle_chain(name):
+def test_chain_matches_oracle_chain(name, fused):
     cfg, scores, bias, ids, w, idx = workload(name)
     down = workload_down(name)
-    pipe = _pipe(cfg)
+    pipe = _pipe(cfg, fused)
     d = torch.from_numpy(down.view(np.int16)).cuda().view(torch.bfloat16)
     out = pipe(torch.from_numpy(scores).cuda(), torch.from_numpy(bias).cuda(), d)
     torch.cuda.synchronize()
@@ -34,6 +35,7 @@ def test_chain_matches_oracle_chain(name):
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert finalize_tolerance_ok(got, ref).all()
     assert np.array_equal(got, f32_to_bf16_bits(ref))
+    assert pipe.device_status() == 0
 
 
 @pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "skewed_ungrouped"])

@@ -149,6 +149,72 @@ def test_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
 
 
+# Segment layout (E = 32 * L, K <= 8, groups of whole lanes): list lengths K < 8,
+# groups spanning several lanes, one group per lane, all groups kept, L = 2 .. 32.
+SEG_SHAPES = [
+    (64, 1, 1, 8), (64, 2, 1, 4), (128, 1, 1, 1), (128, 4, 2, 8), (128, 2, 2, 7),
+    (256, 8, 4, 1), (256, 8, 4, 2), (256, 8, 4, 5), (256, 8, 4, 7), (256, 8, 8, 8),
+    (256, 8, 1, 8), (256, 8, 2, 3), (512, 16, 4, 8), (512, 8, 3, 6), (512, 1, 1, 8),
+    (1024, 32, 4, 8), (1024, 4, 2, 8), (1024, 1, 1, 3),
+]
+
+
+@pytest.mark.parametrize("E,G,M,K", SEG_SHAPES)
+@pytest.mark.parametrize("norm", [True, False])
+def test_segment_layout_shapes(E, G, M, K, norm):
+    rng = np.random.default_rng(E * 131 + G * 17 + M * 5 + K)
+    T = 1003  # not a multiple of the tokens per warp or per CTA
+    scores = rng.random((T, E), dtype=np.float32)
+    bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    assert_route_parity(scores, bias, K, G, M, norm, 2.5)
+
+
+@pytest.mark.parametrize("E,G,M", [(256, 8, 4), (256, 8, 1), (128, 1, 1), (512, 16, 2)])
+def test_segment_one_lane_takes_all(E, G, M):
+    """Every pick comes from one lane's 32 experts, so the (K+1)-th key is
+    that lane's ninth best, found by rescanning its scores."""
+    rng = np.random.default_rng(E + G + M)
+    T, K = 700, 8
+    scores = rng.random((T, E), dtype=np.float32)
+    bias = np.zeros(E, np.float32)
+    bias[40:48] = 1.0          # inside expert block 1 (experts 32 .. 63)
+    bias[40:48] += rng.random(8, dtype=np.float32) * 0.01
+    ids, _ = assert_route_parity(scores, bias, K, G, M, True, 1.0)
+    assert ((ids >= 40) & (ids < 48)).all()
+
+
+@pytest.mark.parametrize("E,G,M,K", [(256, 8, 4, 8), (128, 1, 1, 8), (512, 16, 4, 6),
+                                     (1024, 32, 8, 8)])
+def test_segment_near_equal_scores(E, G, M, K):
+    """Clusters of scores a few ULPs apart, in an order that disagrees with
+    the expert order: the selection keys agree above their index bits, so the
+    tokens take the exact fallback; ids and weights must still be exact."""
+    rng = np.random.default_rng(E * 3 + K)
+    T = 640
+    scores = (rng.random((T, E), dtype=np.float32) * 0.8).astype(np.float32)
+    for t in range(T):
+        members = rng.choice(E, size=12, replace=False)
+        base = np.float32(0.85 + 0.1 * rng.random())
+        steps = rng.permutation(12) * int(rng.integers(1, 20))
+        vals = base.view(np.uint32) + steps.astype(np.uint32)
+        scores[t, members] = vals.view(np.float32)
+    bias = np.zeros(E, np.float32)
+    assert_route_parity(scores, bias, K, G, M, True, 1.0)
+    bias = (rng.integers(-2, 3, size=E) * np.float32(2.0 ** -22)).astype(np.float32)
+    assert_route_parity(scores, bias, K, G, M, False, 1.0)
+
+
+@pytest.mark.parametrize("E,G,M,K", [(128, 1, 1, 8), (256, 8, 4, 8), (512, 16, 4, 8),
+                                     (1024, 32, 4, 8)])
+def test_segment_tie_stress(E, G, M, K):
+    """Scores on a 1/8 grid: nearly every token falls back to the exact path."""
+    rng = np.random.default_rng(E + 5 * K)
+    T = 300
+    scores = (rng.integers(0, 9, size=(T, E)) / 8).astype(np.float32)
+    for bias in (np.zeros(E, np.float32), (rng.integers(-1, 2, size=E) / 8).astype(np.float32)):
+        assert_route_parity(scores, bias, K, G, M, True, 1.0)
+
+
 def gpu_route_sigmoid(logits, bias, K, G, M, norm, scale):
     import moe_token_routing_gb300 as moe
     s = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
@@ -176,7 +242,8 @@ def test_sigmoid_loader_on_workloads(name):
 
 
 @pytest.mark.parametrize("E,G,M,K", [(8, 4, 2, 3), (16, 4, 2, 4), (96, 4, 2, 8), (256, 8, 4, 8),
-                                     (384, 1, 1, 8)])
+                                     (384, 1, 1, 8), (128, 1, 1, 8), (512, 16, 4, 8),
+                                     (1024, 32, 4, 5)])
 def test_sigmoid_loader_shapes_and_extremes(E, G, M, K):
     rng = np.random.default_rng(E + K)
     logits = (rng.standard_normal((300, E)) * 6).astype(np.float32)
