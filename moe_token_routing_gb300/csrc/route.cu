@@ -37,13 +37,17 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
 }
 
 template <int L, bool kGroups>
-__global__ void __launch_bounds__(kRouteThreads, 4) route_seg_kernel(const RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const RouteArgs a) {
   __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
+  __shared__ uint64_t s_cand[kRouteWarps * (32 / L) * kSegCand];
+  __shared__ int s_slot[kRouteWarps * (32 / L) * kSegTop];
   wait_for_prior_grid();
   if (threadIdx.x < 32) stage_seg_bias(a, s_bias);
   __syncthreads();
   const int warps = blockDim.x >> 5;
-  route_tokens_seg<L, kGroups>(a, s_bias, (int64_t)blockIdx.x * warps + (threadIdx.x >> 5),
+  const int warp = threadIdx.x >> 5;
+  route_tokens_seg<L, kGroups>(a, s_bias, s_cand + warp * (32 / L) * kSegCand,
+                               s_slot + warp * (32 / L) * kSegTop, (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps, [](int64_t, int, int) {});
 }
 

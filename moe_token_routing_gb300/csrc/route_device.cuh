@@ -392,12 +392,15 @@ __device__ __forceinline__ void route_tokens_warp(const RouteArgs& a, int64_t fi
 // exact selection whenever the first K+1 keys differ above bit key_bits: then
 // every other candidate's order key is below all K chosen ones and the chosen
 // ones keep their order. Otherwise (two near-equal scores at the top, about
-// 0.4% of the tokens of the prefill workload) the token is routed again by the
-// exact warp path.
+// 0.4% of the tokens of the prefill workload) the segment ranks the few
+// candidates that can still be chosen by their exact 64-bit keys, and only
+// when that set is not known from the lanes' lists is the token routed again
+// by the exact warp path.
 
 constexpr int kSegKeys = 32;        // experts per lane
 constexpr int kSegTop = 8;          // length of the sorted lists (K <= 8)
 constexpr int kSegBiasStride = 36;  // shared-memory floats per lane block of bias
+constexpr int kSegCand = 32;        // tie resolution: candidate keys per token
 
 __device__ __forceinline__ void cmpx_desc(uint32_t& a, uint32_t& b) {
   const uint32_t hi = max(a, b);
@@ -517,20 +520,25 @@ inline int seg_warps_per_cta(int64_t T, int L, int sm_count) {
 }
 
 // Routes the tokens of warps warp_id, warp_id + num_warps, ... (32/L tokens
-// each) with the calling warp; s_bias is the bias from stage_seg_bias. After
-// token t's ids and weights are written, on_id(t, k, id) is called once per
-// k < K. kGroups: topk_group < n_groups (a group spans L/G whole lanes).
+// each) with the calling warp; s_bias is the bias from stage_seg_bias, cand
+// and slot this warp's (32/L) * kSegCand and (32/L) * kSegTop words of shared
+// memory for resolving ties. After token t's ids and weights are written,
+// on_id(t, k, id) is called once per k < K. kGroups: topk_group < n_groups (a
+// group spans L/G whole lanes).
 template <int L, bool kGroups, typename OnId>
 __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float* s_bias,
-                                                 int64_t warp_id, int64_t num_warps,
-                                                 OnId on_id) {
+                                                 uint64_t* cand, int* slot, int64_t warp_id,
+                                                 int64_t num_warps, OnId on_id) {
   static_assert(L >= 2 && L <= 32 && (L & (L - 1)) == 0, "segments of 2 .. 32 lanes");
   constexpr int kTokens = 32 / L;                 // tokens per warp
   constexpr int kOut = (kSegTop + L - 1) / L;     // list entries a lane writes out
   const int lane = threadIdx.x & 31;
   const int j = lane & (L - 1);
   const int seg_base = lane & ~(L - 1);
+  const unsigned seg_mask = (L == 32 ? kFullMask : ((1u << L) - 1u) << seg_base);
   const int e0 = kSegKeys * j;
+  uint64_t* seg_cand = cand + (lane / L) * kSegCand;
+  int* seg_slot = slot + (lane / L) * kSegTop;
   const uint32_t tag0 = a.key_low - (uint32_t)e0;
   const int gl = kGroups ? L / a.G : L;  // lanes per group
   const int grp = j / gl;
@@ -619,7 +627,8 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
     }
 
     // ---- exact unless two of the first K+1 keys agree above bit key_bits ----
-    bool redo = pick8(top, a.K - 1) == 0u;
+    const uint32_t last = pick8(top, a.K - 1);
+    bool redo = last == 0u;
 #pragma unroll
     for (int r = 0; r < kSegTop; ++r) {
       if (r < a.K) {
@@ -628,14 +637,72 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
       }
     }
 
-    // ---- ids and weights (list entries j, j + L, ...) ----
-    const bool write = live && !redo;
+    // ---- ids (list entries j, j + L, ...) ----
     int id[kOut];
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) id[o] = (int)(a.key_low - (pick8(top, j + L * o) & a.key_low));
+
+    // ---- ties: rank the candidates by their exact keys ----
+    // Let h be the high part of the (K+1)-th key, or of the K-th when the
+    // two differ. Every expert of the exact top-K has a high part >= h (the
+    // first K+1 keys all do, and any lower one is below all of them), and in
+    // each lane those experts are a prefix of its sorted list unless the
+    // whole list qualifies at a tie with the (K+1)-th key. Their exact keys
+    // (order key, then expert) give each one's rank, hence its position.
+    bool exact_path = redo && last == 0u;  // fewer than K candidates: the warp path decides
+    if (__any_sync(kFullMask, redo && !exact_path)) {
+      const bool boundary = ((last ^ next) >> a.key_bits) == 0u;
+      const uint32_t h = (boundary ? next : last) >> a.key_bits;
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c += mine[i] != 0u && (mine[i] >> a.key_bits) >= h;
+      const bool over = boundary && c == 8;
+      if (!redo || exact_path) c = 0;
+      int incl = c;  // this lane's end offset in the segment's candidate list
+#pragma unroll
+      for (int off = 1; off < L; off <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, off, L);
+        if (j >= off) incl += y;
+      }
+      const int n = __shfl_sync(kFullMask, incl, seg_base + L - 1);
+      // (the ballot is taken by every lane, outside any short-circuit test)
+      const unsigned over_lanes = __ballot_sync(kFullMask, over);
+      const bool ok = redo && !exact_path && n <= kSegCand && (over_lanes & seg_mask) == 0u;
+      if (!ok) c = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i < c) {
+          const int e = (int)(a.key_low - (mine[i] & a.key_low));
+          const float b = __fadd_rn(apply_score_fn(a.score_fn, __ldg(row + e)), bias_j[e - e0]);
+          const uint32_t u = __float_as_uint(b);
+          const uint32_t tk = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+          seg_cand[incl - c + i] = ((uint64_t)tk << 32) | (a.key_low - (uint32_t)e);
+        }
+      }
+      __syncwarp();
+      const int c_max = __reduce_max_sync(kFullMask, c);
+      for (int i = 0; i < c_max; ++i) {
+        if (i < c) {
+          const uint64_t x = seg_cand[incl - c + i];
+          int r = 0;
+          for (int m = 0; m < n; ++m) r += seg_cand[m] > x;  // keys are distinct
+          if (r < a.K) seg_slot[r] = (int)(a.key_low - (uint32_t)(x & 0xffffffffull));
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int o = 0; o < kOut; ++o)
+        if (ok && j + L * o < a.K) id[o] = seg_slot[j + L * o];
+      __syncwarp();  // the candidate and slot words are reused by the next tokens
+      exact_path = exact_path || (redo && !ok);
+    }
+
+    // ---- weights ----
+    const bool write = live && !exact_path;
     float w[kOut];
 #pragma unroll
     for (int o = 0; o < kOut; ++o) {
       const int k = j + L * o;
-      id[o] = (int)(a.key_low - (pick8(top, k) & a.key_low));
       w[o] = 0.0f;
       if (write && k < a.K) w[o] = apply_score_fn(a.score_fn, __ldg(row + id[o]));
     }
@@ -657,8 +724,8 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
       }
     }
 
-    // ---- tokens whose top keys tied: the exact warp path, one token at a time ----
-    unsigned pending = __ballot_sync(kFullMask, live && redo && j == 0);
+    // ---- tokens the ranking could not settle: the exact warp path, one at a time ----
+    unsigned pending = __ballot_sync(kFullMask, live && exact_path && j == 0);
     while (pending) {
       const int l0 = __ffs(pending) - 1;
       pending &= pending - 1;

@@ -525,14 +525,18 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2)
 }
 
 template <int L, bool kGroups>
-__global__ void __launch_bounds__(kRouteThreads, 4) route_count_seg_kernel(const CountRouteArgs c) {
+__global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const CountRouteArgs c) {
   __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
+  __shared__ uint64_t s_cand[kRouteWarps * (32 / L) * kSegCand];
+  __shared__ int s_slot[kRouteWarps * (32 / L) * kSegTop];
   wait_for_prior_grid();
   if (threadIdx.x < 32) stage_seg_bias(c.r, s_bias);
   __syncthreads();
   const int warps = blockDim.x >> 5;
   const int64_t K = c.r.K;
-  route_tokens_seg<L, kGroups>(c.r, s_bias, (int64_t)blockIdx.x * warps + (threadIdx.x >> 5),
+  const int warp = threadIdx.x >> 5;
+  route_tokens_seg<L, kGroups>(c.r, s_bias, s_cand + warp * (32 / L) * kSegCand,
+                               s_slot + warp * (32 / L) * kSegTop, (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps,
                                [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
 }
