@@ -317,8 +317,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
 
     K = args.steps
     # Timed region: events only at the step start, before finalize and at the
-    # step end, so the route -> create_indices launches (or the fused
-    # route_index launch) and finalize chain back to back.
+    # step end, so the route_index launches (router, rows, scatter; or route
+    # -> create_indices with --separate-index) and finalize chain back to back.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(device_uuid(dev))
     sampler.start()
@@ -366,7 +366,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     route_ms = [e[0].elapsed_time(e[1]) for e in sev]
     index_ms = [e[1].elapsed_time(e[2]) for e in sev]
     fin_stage_ms = [e[2].elapsed_time(e[3]) for e in sev]
-    # the fused launch as a stage of its own
+    # moe_route_index (the steps' default route + index) as a stage of its own
     for i in range(ks):
         flush_l2()
         e = sev[i]

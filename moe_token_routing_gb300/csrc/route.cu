@@ -18,7 +18,7 @@
 //    order-preserving integer keys) where ties resolve to the lowest lane,
 //    which holds the lowest expert index, because lanes hold ascending ranges.
 //  * E <= 32: one thread per token, all E scores in registers.
-// Both read each score row once with coalesced (vector) loads, keep the bias
+// All three read each score row once with 16-byte (or scalar) loads, keep the bias
 // in registers across a persistent token loop, and write K ids and weights
 // per token.
 #include "route_device.cuh"

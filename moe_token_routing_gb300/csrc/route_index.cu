@@ -1,5 +1,5 @@
-// Fused router + expert index builder for sm_103a: one cooperative launch
-// that computes what moe_route followed by moe_create_indices computes.
+// Router + expert index builder for sm_103a: what moe_route followed by
+// moe_create_indices computes, in two designs.
 //
 // Page "group_limited_router_kernel" fixes the routing (description
 // paragraph; Args expert_indices, expert_weights); page "moe_create_indices"
@@ -7,6 +7,12 @@
 // permutation and the usage stats (description paragraph; Args
 // token_expert_order .. expert_usage_stats, scales_offset_p).
 //
+// moe_route_index (three launches, at the end of this file): the router adds
+// each slot it writes to counts[expert][slot / 1024], and the index builder's
+// row-prefix and scatter kernels (index_device.cuh) follow, so the separate
+// count kernel and its re-read of the ids disappear.
+//
+// moe_route_index_single_launch (one cooperative launch, described here):
 // CTA b owns a contiguous range of tokens and each of its warps a contiguous
 // part of that range, so the slots t*K+k of a warp form one contiguous slot
 // range and a stable placement needs only per-warp counts:
