@@ -1,0 +1,58 @@
+"""Host logic of bench.py that needs no GPU: the hash-gated ncu traffic figure
+and the command-line defaults."""
+import hashlib
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _tree(tmp_path, kernel_text, summary_hash, dram="2090510848"):
+    src = tmp_path / "moe_token_routing_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text(kernel_text)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "k_summary.txt").write_text(
+        "# a comment: with a colon\n"
+        f"dram_bytes_per_launch: {dram}\n"
+        f"source_sha256_16: {summary_hash}\n")
+
+
+def test_traffic_reported_only_for_the_profiled_source(tmp_path, monkeypatch):
+    import bench
+    text = "__global__ void k() {}\n"
+    digest = hashlib.sha256(text.encode()).hexdigest()[:16]
+    _tree(tmp_path, text, digest)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("k.cu", "k_summary.txt") == 2090510848
+    # the kernel changed after the capture: no traffic figure
+    (tmp_path / "moe_token_routing_gb300" / "csrc" / "k.cu").write_text(text + "// edited\n")
+    assert bench.profile_traffic("k.cu", "k_summary.txt") is None
+
+
+def test_traffic_missing_summary_is_none(tmp_path, monkeypatch):
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("finalize.cu", "absent.txt") is None
+
+
+def test_committed_finalize_summary_matches_the_source():
+    """The committed finalize summary carries the hash of the current
+    finalize.cu, so the bench line's roofline.traffic is not null."""
+    import bench
+    assert bench.profile_traffic("finalize.cu", "finalize_dsv3_prefill.txt") is not None
+
+
+def test_default_arguments(monkeypatch):
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse_args()
+    assert a.gpus == 1 and a.impl == "gb300" and a.config == "dsv3_prefill"
+    assert a.warmup >= 3 and not a.separate_index
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--separate-index", "--steps", "7"])
+    a = bench.parse_args()
+    assert a.separate_index and a.steps == 7
