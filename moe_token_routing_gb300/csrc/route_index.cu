@@ -512,9 +512,17 @@ struct CountRouteArgs {
   int row;
 };
 
+// Adds one to the count word of (id, slot's chunk). The lanes of the warp
+// that are here together and add to the same word combine first (one atomic
+// of their number): with few or skewed experts, hundreds of slots of a chunk
+// land on the same word, and serialised atomics on it cost more than the
+// routing. Which lanes combine does not change the sum.
 __device__ __forceinline__ void count_slot(const CountRouteArgs& c, int64_t slot, int id) {
-  if (c.counts != nullptr && (unsigned)id < (unsigned)c.r.E)
-    atomicAdd(c.counts + (int64_t)id * c.row + slot / kSlotsPerCta, 1u);
+  if (c.counts == nullptr || (unsigned)id >= (unsigned)c.r.E) return;
+  uint32_t* word = c.counts + (int64_t)id * c.row + slot / kSlotsPerCta;
+  const unsigned here = __activemask();
+  const unsigned same = __match_any_sync(here, reinterpret_cast<unsigned long long>(word));
+  if ((int)(threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(word, (uint32_t)__popc(same));
 }
 
 template <int C, bool kVec, bool kSoftmax>
