@@ -36,8 +36,9 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2) route_warp_kern
                              [](int64_t, int, int) {});
 }
 
-template <int L, bool kGroups>
+template <int L, bool kGroups, bool kSoftmax>
 __global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const RouteArgs a) {
+  extern __shared__ float dyn_smem[];  // softmax loader: a.warp_smem_words per warp
   __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
   __shared__ uint64_t s_cand[kRouteWarps * (32 / L) * kSegCand];
   __shared__ int s_slot[kRouteWarps * (32 / L) * kSegTop];
@@ -46,8 +47,10 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const Route
   __syncthreads();
   const int warps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
-  route_tokens_seg<L, kGroups>(a, s_bias, s_cand + warp * (32 / L) * kSegCand,
-                               s_slot + warp * (32 / L) * kSegTop, (int64_t)blockIdx.x * warps + warp,
+  route_tokens_seg<L, kGroups, kSoftmax>(a, s_bias, s_cand + warp * (32 / L) * kSegCand,
+                               s_slot + warp * (32 / L) * kSegTop,
+                               kSoftmax ? dyn_smem + warp * a.warp_smem_words : nullptr,
+                               (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps, [](int64_t, int, int) {});
 }
 
@@ -92,13 +95,22 @@ moe_status_t launch_warp_path(const RoutePlan& p, cudaStream_t stream) {
   return launch_warp_path_fn<C, false>(p, stream);
 }
 
-template <int L>
-moe_status_t launch_seg_path(const RoutePlan& p, cudaStream_t stream) {
+template <int L, bool kSoftmax>
+moe_status_t launch_seg_path_fn(const RoutePlan& p, cudaStream_t stream) {
   const int warps = seg_warps_per_cta(p.a.T, L, device_info().sm_count);
   const int64_t tokens_per_cta = (int64_t)warps * (32 / L);
+  const size_t smem = kSoftmax ? route_warp_smem(p, warps) : 0;
   if (p.a.group_mode == kGroupsAllKept)
-    return launch_route(route_seg_kernel<L, false>, p.a, tokens_per_cta, 0, stream, 32 * warps);
-  return launch_route(route_seg_kernel<L, true>, p.a, tokens_per_cta, 0, stream, 32 * warps);
+    return launch_route(route_seg_kernel<L, false, kSoftmax>, p.a, tokens_per_cta, smem, stream,
+                        32 * warps);
+  return launch_route(route_seg_kernel<L, true, kSoftmax>, p.a, tokens_per_cta, smem, stream,
+                      32 * warps);
+}
+
+template <int L>
+moe_status_t launch_seg_path(const RoutePlan& p, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_seg_path_fn<L, true>(p, stream);
+  return launch_seg_path_fn<L, false>(p, stream);
 }
 
 template <int EP>

@@ -448,21 +448,32 @@ __device__ __forceinline__ uint32_t selection_key(const RouteArgs& a, float b, u
   return (k & ~a.key_low) | tag;
 }
 
-// Biased scores of this lane's 32 experts of row t (score function applied).
-__device__ __forceinline__ void load_seg_scores(const RouteArgs& a, const float* row,
-                                                const float* bias_j, float (&b)[kSegKeys]) {
+// The routing score of one expert from its loaded value x: the score
+// function, or for the softmax loader exp(x - m) / sum with the row's max m
+// and its sum in ascending expert order. These are the operations the whole
+// row goes through, so the result has the same bits.
+template <bool kSoftmax>
+__device__ __forceinline__ float seg_score(const RouteArgs& a, float x, float m, float sum) {
+  if constexpr (kSoftmax)
+    return __fdiv_rn(score_exp_f32(__fsub_rn(x, m)), sum);
+  else
+    return apply_score_fn(a.score_fn, x);
+}
+
+// This lane's 32 loaded values of a row (16-byte loads).
+__device__ __forceinline__ void load_seg_row(const float* row, float (&x)[kSegKeys]) {
 #pragma unroll
   for (int q = 0; q < kSegKeys / 4; ++q) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
-    b[4 * q + 0] = v.x;
-    b[4 * q + 1] = v.y;
-    b[4 * q + 2] = v.z;
-    b[4 * q + 3] = v.w;
+    x[4 * q + 0] = v.x;
+    x[4 * q + 1] = v.y;
+    x[4 * q + 2] = v.z;
+    x[4 * q + 3] = v.w;
   }
-  if (a.score_fn != MOE_SCORES_AS_GIVEN) {
-#pragma unroll
-    for (int i = 0; i < kSegKeys; ++i) b[i] = apply_score_fn(a.score_fn, b[i]);
-  }
+}
+
+// b := scores + bias, in place (b holds scores on entry).
+__device__ __forceinline__ void add_seg_bias(const float* bias_j, float (&b)[kSegKeys]) {
 #pragma unroll
   for (int q = 0; q < kSegKeys / 4; ++q) {
     const float4 c = *reinterpret_cast<const float4*>(bias_j + 4 * q);
@@ -503,10 +514,11 @@ __device__ __forceinline__ void stage_seg_bias(const RouteArgs& a, float* s_bias
 
 // The exact warp path for one token, out of line: it runs for few tokens, and
 // keeping it out of the segment loop keeps that loop's code small.
-template <int L, typename OnId>
-__device__ __noinline__ void route_one_token_exact(const RouteArgs a, int64_t t, OnId on_id) {
+template <int L, bool kSoftmax, typename OnId>
+__device__ __noinline__ void route_one_token_exact(const RouteArgs a, int64_t t, float* warp_smem,
+                                                   OnId on_id) {
   // (the warp path's vector loads need C = L to be a multiple of 4)
-  route_tokens_warp<L, L % 4 == 0, false>(a, t, t + 1, 1, nullptr, on_id);
+  route_tokens_warp<L, L % 4 == 0, kSoftmax>(a, t, t + 1, 1, warp_smem, on_id);
 }
 
 // Warps per CTA of a segment-layout launch: 8, or fewer when 8-warp CTAs
@@ -522,13 +534,17 @@ inline int seg_warps_per_cta(int64_t T, int L, int sm_count) {
 // Routes the tokens of warps warp_id, warp_id + num_warps, ... (32/L tokens
 // each) with the calling warp; s_bias is the bias from stage_seg_bias, cand
 // and slot this warp's (32/L) * kSegCand and (32/L) * kSegTop words of shared
-// memory for resolving ties. After token t's ids and weights are written,
+// memory for resolving ties, warp_smem its a.warp_smem_words floats for the
+// warp path's softmax strip. After token t's ids and weights are written,
 // on_id(t, k, id) is called once per k < K. kGroups: topk_group < n_groups (a
-// group spans L/G whole lanes).
-template <int L, bool kGroups, typename OnId>
+// group spans L/G whole lanes). kSoftmax: the softmax loader, whose sum runs
+// in ascending expert order by handing the running sum from lane to lane of
+// the segment (the order of a sequential loop, so the same bits).
+template <int L, bool kGroups, bool kSoftmax, typename OnId>
 __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float* s_bias,
-                                                 uint64_t* cand, int* slot, int64_t warp_id,
-                                                 int64_t num_warps, OnId on_id) {
+                                                 uint64_t* cand, int* slot, float* warp_smem,
+                                                 int64_t warp_id, int64_t num_warps,
+                                                 OnId on_id) {
   static_assert(L >= 2 && L <= 32 && (L & (L - 1)) == 0, "segments of 2 .. 32 lanes");
   constexpr int kTokens = 32 / L;                 // tokens per warp
   constexpr int kOut = (kSegTop + L - 1) / L;     // list entries a lane writes out
@@ -552,9 +568,34 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
     // ---- selection keys, the group's top-2 and this lane's sorted top-8 ----
     uint32_t key[4][8];
     float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+    float smax = 0.0f, ssum = 1.0f;  // the softmax loader's row max and sum
     {
       float b[kSegKeys];
-      load_seg_scores(a, row + e0, bias_j, b);
+      load_seg_row(row + e0, b);
+      if constexpr (kSoftmax) {
+        smax = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) smax = fmaxf(smax, b[i]);
+#pragma unroll
+        for (int off = 1; off < L; off <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFullMask, smax, off));
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) b[i] = score_exp_f32(__fsub_rn(b[i], smax));
+        float run = 0.0f;
+        for (int l = 0; l < L; ++l) {
+          if (j == l) {
+#pragma unroll
+            for (int i = 0; i < kSegKeys; ++i) run = __fadd_rn(run, b[i]);
+          }
+          run = __shfl_sync(kFullMask, run, seg_base + l);
+        }
+        ssum = run;
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) b[i] = __fdiv_rn(b[i], ssum);
+      } else if (a.score_fn != MOE_SCORES_AS_GIVEN) {
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) b[i] = apply_score_fn(a.score_fn, b[i]);
+      }
+      add_seg_bias(bias_j, b);
 #pragma unroll
       for (int i = 0; i < kSegKeys; ++i) {
         key[i / 8][i % 8] = selection_key(a, b[i], tag0 - (uint32_t)i);
@@ -615,7 +656,10 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
         // all eight of this lane's listed keys were chosen: its next key is
         // the best of the other 24, recomputed from the scores
         float b[kSegKeys];
-        load_seg_scores(a, row + e0, bias_j, b);
+        load_seg_row(row + e0, b);
+#pragma unroll
+        for (int i = 0; i < kSegKeys; ++i) b[i] = seg_score<kSoftmax>(a, b[i], smax, ssum);
+        add_seg_bias(bias_j, b);
 #pragma unroll
         for (int i = 0; i < kSegKeys; ++i) {
           const uint32_t k = selection_key(a, b[i], tag0 - (uint32_t)i);
@@ -673,7 +717,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
       for (int i = 0; i < 8; ++i) {
         if (i < c) {
           const int e = (int)(a.key_low - (mine[i] & a.key_low));
-          const float b = __fadd_rn(apply_score_fn(a.score_fn, __ldg(row + e)), bias_j[e - e0]);
+          const float b = __fadd_rn(seg_score<kSoftmax>(a, __ldg(row + e), smax, ssum), bias_j[e - e0]);
           const uint32_t u = __float_as_uint(b);
           const uint32_t tk = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
           seg_cand[incl - c + i] = ((uint64_t)tk << 32) | (a.key_low - (uint32_t)e);
@@ -704,7 +748,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
     for (int o = 0; o < kOut; ++o) {
       const int k = j + L * o;
       w[o] = 0.0f;
-      if (write && k < a.K) w[o] = apply_score_fn(a.score_fn, __ldg(row + id[o]));
+      if (write && k < a.K) w[o] = seg_score<kSoftmax>(a, __ldg(row + id[o]), smax, ssum);
     }
     if (a.norm) {
       float sum = 0.0f;
@@ -730,7 +774,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
       const int l0 = __ffs(pending) - 1;
       pending &= pending - 1;
       const int64_t tr = base + l0 / L;
-      route_one_token_exact<L>(a, tr, on_id);
+      route_one_token_exact<L, kSoftmax>(a, tr, warp_smem, on_id);
     }
   }
 }
@@ -933,7 +977,6 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   // fallback
   const int L = E / kSegKeys;
   if (E == kSegKeys * p->C && K <= kSegTop && p->vec && aligned(expert_bias, 16) &&
-      score_fn != MOE_SCORES_SOFTMAX &&
       (a.group_mode == kGroupsAllKept || (a.group_mode == kGroupsSegment && G <= L && L % G == 0)))
     p->seg = L;
   return MOE_OK;

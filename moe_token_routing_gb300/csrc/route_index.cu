@@ -538,8 +538,9 @@ __global__ void __launch_bounds__(kRouteThreads, C <= 8 ? 4 : 2)
       [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
 }
 
-template <int L, bool kGroups>
+template <int L, bool kGroups, bool kSoftmax>
 __global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const CountRouteArgs c) {
+  extern __shared__ float dyn_smem[];  // softmax loader: c.r.warp_smem_words per warp
   __shared__ __align__(16) float s_bias[kSegBiasStride * (MOE_MAX_EXPERTS / kSegKeys)];
   __shared__ uint64_t s_cand[kRouteWarps * (32 / L) * kSegCand];
   __shared__ int s_slot[kRouteWarps * (32 / L) * kSegTop];
@@ -549,8 +550,10 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const
   const int warps = blockDim.x >> 5;
   const int64_t K = c.r.K;
   const int warp = threadIdx.x >> 5;
-  route_tokens_seg<L, kGroups>(c.r, s_bias, s_cand + warp * (32 / L) * kSegCand,
-                               s_slot + warp * (32 / L) * kSegTop, (int64_t)blockIdx.x * warps + warp,
+  route_tokens_seg<L, kGroups, kSoftmax>(c.r, s_bias, s_cand + warp * (32 / L) * kSegCand,
+                               s_slot + warp * (32 / L) * kSegTop,
+                               kSoftmax ? dyn_smem + warp * c.r.warp_smem_words : nullptr,
+                               (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps,
                                [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
 }
@@ -634,15 +637,23 @@ moe_status_t launch_count_thread(const RoutePlan& p, const CountRouteArgs& c,
                                 stream);
 }
 
-template <int L>
-moe_status_t launch_count_seg(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
+template <int L, bool kSoftmax>
+moe_status_t launch_count_seg_fn(const RoutePlan& p, const CountRouteArgs& c,
+                                 cudaStream_t stream) {
   const int warps = seg_warps_per_cta(c.r.T, L, device_info().sm_count);
   const int64_t tokens_per_cta = (int64_t)warps * (32 / L);
+  const size_t smem = kSoftmax ? route_warp_smem(p, warps) : 0;
   if (p.a.group_mode == kGroupsAllKept)
-    return launch_counting_router(route_count_seg_kernel<L, false>, c, c.r.T, tokens_per_cta, 0,
-                                  stream, 32 * warps);
-  return launch_counting_router(route_count_seg_kernel<L, true>, c, c.r.T, tokens_per_cta, 0,
-                                stream, 32 * warps);
+    return launch_counting_router(route_count_seg_kernel<L, false, kSoftmax>, c, c.r.T,
+                                  tokens_per_cta, smem, stream, 32 * warps);
+  return launch_counting_router(route_count_seg_kernel<L, true, kSoftmax>, c, c.r.T,
+                                tokens_per_cta, smem, stream, 32 * warps);
+}
+
+template <int L>
+moe_status_t launch_count_seg(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX) return launch_count_seg_fn<L, true>(p, c, stream);
+  return launch_count_seg_fn<L, false>(p, c, stream);
 }
 
 moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
