@@ -22,6 +22,7 @@
 // in registers across a persistent token loop, and write K ids and weights
 // per token.
 #include "route_device.cuh"
+#include "route_quad.cuh"
 
 namespace moe {
 namespace {
@@ -52,6 +53,14 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const Route
                                kSoftmax ? dyn_smem + warp * a.warp_smem_words : nullptr,
                                (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps, [](int64_t, int, int) {});
+}
+
+template <int P, bool kSigmoid>
+__global__ void __launch_bounds__(kQuadThreadsMax, 1) route_quad_kernel(const RouteArgs a,
+                                                                       int depth) {
+  extern __shared__ __align__(128) char quad_smem_buf[];
+  wait_for_prior_grid();
+  route_tokens_quad<P, kSigmoid>(a, quad_smem_buf, depth, [](int64_t, int, int) {});
 }
 
 template <int EP, bool kVec>
@@ -113,6 +122,13 @@ moe_status_t launch_seg_path(const RoutePlan& p, cudaStream_t stream) {
   return launch_seg_path_fn<L, false>(p, stream);
 }
 
+template <int P>
+moe_status_t launch_quad_path(const RoutePlan& p, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SIGMOID)
+    return launch_quad(route_quad_kernel<P, true>, p.a, p.a.T, p.a.E, stream);
+  return launch_quad(route_quad_kernel<P, false>, p.a, p.a.T, p.a.E, stream);
+}
+
 template <int EP>
 moe_status_t launch_thread_path(const RoutePlan& p, cudaStream_t stream) {
   if (p.vec) return launch_route(route_thread_kernel<EP, true>, p.a, kRouteThreads, 0, stream);
@@ -132,6 +148,12 @@ moe_status_t route_impl(int32_t* expert_indices, float* expert_weights,
   if (num_tokens == 0) return MOE_OK;
   st = check_route_pointers(p.a);
   if (st != MOE_OK) return st;
+  switch (p.quad) {
+    case 1: return launch_quad_path<1>(p, stream);
+    case 2: return launch_quad_path<2>(p, stream);
+    case 4: return launch_quad_path<4>(p, stream);
+    default: break;
+  }
   switch (p.seg) {
     case 2: return launch_seg_path<2>(p, stream);
     case 4: return launch_seg_path<4>(p, stream);

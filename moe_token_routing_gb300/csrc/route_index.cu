@@ -43,6 +43,7 @@
 // MOE_DEVICE_STATUS_SYNC_TIMEOUT and skips the phases that depend on it.
 #include "index_device.cuh"
 #include "route_device.cuh"
+#include "route_quad.cuh"
 #include "tagged_sync.cuh"
 
 namespace moe {
@@ -517,12 +518,17 @@ struct CountRouteArgs {
 // of their number): with few or skewed experts, hundreds of slots of a chunk
 // land on the same word, and serialised atomics on it cost more than the
 // routing. Which lanes combine does not change the sum.
-__device__ __forceinline__ void count_slot(const CountRouteArgs& c, int64_t slot, int id) {
-  if (c.counts == nullptr || (unsigned)id >= (unsigned)c.r.E) return;
-  uint32_t* word = c.counts + (int64_t)id * c.row + slot / kSlotsPerCta;
+__device__ __forceinline__ void count_slot(uint32_t* counts, int row, int E, int64_t slot,
+                                           int id) {
+  if (counts == nullptr || (unsigned)id >= (unsigned)E) return;
+  uint32_t* word = counts + (int64_t)id * row + slot / kSlotsPerCta;
   const unsigned here = __activemask();
   const unsigned same = __match_any_sync(here, reinterpret_cast<unsigned long long>(word));
   if ((int)(threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(word, (uint32_t)__popc(same));
+}
+
+__device__ __forceinline__ void count_slot(const CountRouteArgs& c, int64_t slot, int id) {
+  count_slot(c.counts, c.row, c.r.E, slot, id);
 }
 
 template <int C, bool kVec, bool kSoftmax>
@@ -556,6 +562,19 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const
                                (int64_t)blockIdx.x * warps + warp,
                                (int64_t)gridDim.x * warps,
                                [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
+}
+
+template <int P, bool kSigmoid>
+__global__ void __launch_bounds__(kQuadThreadsMax, 1)
+    route_count_quad_kernel(const CountRouteArgs c, int depth) {
+  extern __shared__ __align__(128) char quad_smem_buf[];
+  wait_for_prior_grid();
+  uint32_t* const counts = c.counts;
+  const int row = c.row, E = c.r.E;
+  const int64_t K = c.r.K;
+  route_tokens_quad<P, kSigmoid>(c.r, quad_smem_buf, depth, [=](int64_t t, int k, int id) {
+    count_slot(counts, row, E, t * K + k, id);
+  });
 }
 
 template <int EP, bool kVec>
@@ -656,8 +675,21 @@ moe_status_t launch_count_seg(const RoutePlan& p, const CountRouteArgs& c, cudaS
   return launch_count_seg_fn<L, false>(p, c, stream);
 }
 
+template <int P>
+moe_status_t launch_count_quad(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SIGMOID)
+    return launch_quad(route_count_quad_kernel<P, true>, c, c.r.T, c.r.E, stream);
+  return launch_quad(route_count_quad_kernel<P, false>, c, c.r.T, c.r.E, stream);
+}
+
 moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
                                    cudaStream_t stream) {
+  switch (p.quad) {
+    case 1: return launch_count_quad<1>(p, c, stream);
+    case 2: return launch_count_quad<2>(p, c, stream);
+    case 4: return launch_count_quad<4>(p, c, stream);
+    default: break;
+  }
   switch (p.seg) {
     case 2: return launch_count_seg<2>(p, c, stream);
     case 4: return launch_count_seg<4>(p, c, stream);
