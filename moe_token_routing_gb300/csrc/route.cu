@@ -22,7 +22,7 @@
 // in registers across a persistent token loop, and write K ids and weights
 // per token.
 #include "route_device.cuh"
-#include "route_quad.cuh"
+#include "route_staged.cuh"
 
 namespace moe {
 namespace {
@@ -55,12 +55,14 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const Route
                                (int64_t)gridDim.x * warps, [](int64_t, int, int) {});
 }
 
-template <int P, bool kSigmoid>
-__global__ void __launch_bounds__(kQuadThreadsMax, 1) route_quad_kernel(const RouteArgs a,
-                                                                       int depth) {
-  extern __shared__ __align__(128) char quad_smem_buf[];
+// kKc: K fixed at compile time (8, the common case), or 0 for any K <= 8.
+template <int G, bool kSigmoid, int kKc>
+__global__ void __launch_bounds__(kStagedThreadsMax, 1) route_staged_kernel(const RouteArgs a,
+                                                                           const StagedSplit sp) {
+  extern __shared__ __align__(128) char staged_smem_buf[];
   wait_for_prior_grid();
-  route_tokens_quad<P, kSigmoid>(a, quad_smem_buf, depth, [](int64_t, int, int) {});
+  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc>(a, staged_smem_buf, sp,
+                                                              [](int64_t, int, int) {});
 }
 
 template <int EP, bool kVec>
@@ -122,11 +124,19 @@ moe_status_t launch_seg_path(const RoutePlan& p, cudaStream_t stream) {
   return launch_seg_path_fn<L, false>(p, stream);
 }
 
-template <int P>
-moe_status_t launch_quad_path(const RoutePlan& p, cudaStream_t stream) {
-  if (p.a.score_fn == MOE_SCORES_SIGMOID)
-    return launch_quad(route_quad_kernel<P, true>, p.a, p.a.T, p.a.E, stream);
-  return launch_quad(route_quad_kernel<P, false>, p.a, p.a.T, p.a.E, stream);
+template <int G, bool kSigmoid>
+moe_status_t launch_staged_path_fn(const RoutePlan& p, cudaStream_t stream) {
+  constexpr int kTok = 32 / kStagedR;
+  if (p.a.K == kSegTop)
+    return launch_staged(route_staged_kernel<G, kSigmoid, kSegTop>, p.a, p.a.T, p.a.E, kTok,
+                         stream);
+  return launch_staged(route_staged_kernel<G, kSigmoid, 0>, p.a, p.a.T, p.a.E, kTok, stream);
+}
+
+template <int G>
+moe_status_t launch_staged_path(const RoutePlan& p, cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SIGMOID) return launch_staged_path_fn<G, true>(p, stream);
+  return launch_staged_path_fn<G, false>(p, stream);
 }
 
 template <int EP>
@@ -148,10 +158,10 @@ moe_status_t route_impl(int32_t* expert_indices, float* expert_weights,
   if (num_tokens == 0) return MOE_OK;
   st = check_route_pointers(p.a);
   if (st != MOE_OK) return st;
-  switch (p.quad) {
-    case 1: return launch_quad_path<1>(p, stream);
-    case 2: return launch_quad_path<2>(p, stream);
-    case 4: return launch_quad_path<4>(p, stream);
+  switch (p.staged) {
+    case 4: return launch_staged_path<4>(p, stream);
+    case 8: return launch_staged_path<8>(p, stream);
+    case 16: return launch_staged_path<16>(p, stream);
     default: break;
   }
   switch (p.seg) {

@@ -913,8 +913,7 @@ struct RoutePlan {
   int EP;   // thread path: E rounded up to 8, 16 or 32
   bool vec; // 16-byte score loads (E % 4 == 0 and a 16-byte aligned score matrix)
   int seg;  // segment layout: lanes per token (E = 32 * seg); 0 when it does not apply
-  int quad; // quad layout: groups per thread in its first pass (E = 128 * quad); 0 when it
-            // does not apply
+  int staged; // staged layout: the number of groups G (E = 32 * G); 0 when it does not apply
 };
 
 // Checks the router's sizes and options and fills `p` (pointers are taken as
@@ -958,7 +957,7 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   while ((1 << a.key_bits) < E) ++a.key_bits;
   a.key_low = (1u << a.key_bits) - 1u;
   p->seg = 0;
-  p->quad = 0;
+  p->staged = 0;
   p->vec = (E % 4 == 0) && aligned(expert_scores, 16);
   p->C = 0;
   p->EP = E <= 8 ? 8 : E <= 16 ? 16 : 32;
@@ -982,12 +981,12 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   if (E == kSegKeys * p->C && K <= kSegTop && p->vec && aligned(expert_bias, 16) &&
       (a.group_mode == kGroupsAllKept || (a.group_mode == kGroupsSegment && G <= L && L % G == 0)))
     p->seg = L;
-  // the quad layout: groups of 32 experts, G = 4, 8 or 16, K <= 8, 16-byte
+  // the staged layout: groups of 32 experts, G = 4, 8 or 16, K <= 8, 16-byte
   // loads and bias, a per-element score loader (the softmax loader needs the
   // whole row's sum and stays on the segment layout)
   if (S == 32 && (G == 4 || G == 8 || G == 16) && K <= kSegTop && p->vec &&
       aligned(expert_bias, 16) && score_fn != MOE_SCORES_SOFTMAX)
-    p->quad = G / 4;
+    p->staged = G;
   return MOE_OK;
 }
 

@@ -43,7 +43,7 @@
 // MOE_DEVICE_STATUS_SYNC_TIMEOUT and skips the phases that depend on it.
 #include "index_device.cuh"
 #include "route_device.cuh"
-#include "route_quad.cuh"
+#include "route_staged.cuh"
 #include "tagged_sync.cuh"
 
 namespace moe {
@@ -564,17 +564,18 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const
                                [&](int64_t t, int k, int id) { count_slot(c, t * K + k, id); });
 }
 
-template <int P, bool kSigmoid>
-__global__ void __launch_bounds__(kQuadThreadsMax, 1)
-    route_count_quad_kernel(const CountRouteArgs c, int depth) {
-  extern __shared__ __align__(128) char quad_smem_buf[];
+// kKc: K fixed at compile time (8, the common case), or 0 for any K <= 8.
+template <int G, bool kSigmoid, int kKc>
+__global__ void __launch_bounds__(kStagedThreadsMax, 1)
+    route_count_staged_kernel(const CountRouteArgs c, const StagedSplit sp) {
+  extern __shared__ __align__(128) char staged_smem_buf[];
   wait_for_prior_grid();
   uint32_t* const counts = c.counts;
   const int row = c.row, E = c.r.E;
   const int64_t K = c.r.K;
-  route_tokens_quad<P, kSigmoid>(c.r, quad_smem_buf, depth, [=](int64_t t, int k, int id) {
-    count_slot(counts, row, E, t * K + k, id);
-  });
+  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc>(
+      c.r, staged_smem_buf, sp,
+      [=](int64_t t, int k, int id) { count_slot(counts, row, E, t * K + k, id); });
 }
 
 template <int EP, bool kVec>
@@ -675,19 +676,28 @@ moe_status_t launch_count_seg(const RoutePlan& p, const CountRouteArgs& c, cudaS
   return launch_count_seg_fn<L, false>(p, c, stream);
 }
 
-template <int P>
-moe_status_t launch_count_quad(const RoutePlan& p, const CountRouteArgs& c, cudaStream_t stream) {
-  if (p.a.score_fn == MOE_SCORES_SIGMOID)
-    return launch_quad(route_count_quad_kernel<P, true>, c, c.r.T, c.r.E, stream);
-  return launch_quad(route_count_quad_kernel<P, false>, c, c.r.T, c.r.E, stream);
+template <int G, bool kSigmoid>
+moe_status_t launch_count_staged_fn(const CountRouteArgs& c, cudaStream_t stream) {
+  constexpr int kTok = 32 / kStagedR;
+  if (c.r.K == kSegTop)
+    return launch_staged(route_count_staged_kernel<G, kSigmoid, kSegTop>, c, c.r.T, c.r.E, kTok,
+                         stream);
+  return launch_staged(route_count_staged_kernel<G, kSigmoid, 0>, c, c.r.T, c.r.E, kTok, stream);
+}
+
+template <int G>
+moe_status_t launch_count_staged(const RoutePlan& p, const CountRouteArgs& c,
+                                 cudaStream_t stream) {
+  if (p.a.score_fn == MOE_SCORES_SIGMOID) return launch_count_staged_fn<G, true>(c, stream);
+  return launch_count_staged_fn<G, false>(c, stream);
 }
 
 moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
                                    cudaStream_t stream) {
-  switch (p.quad) {
-    case 1: return launch_count_quad<1>(p, c, stream);
-    case 2: return launch_count_quad<2>(p, c, stream);
-    case 4: return launch_count_quad<4>(p, c, stream);
+  switch (p.staged) {
+    case 4: return launch_count_staged<4>(p, c, stream);
+    case 8: return launch_count_staged<8>(p, c, stream);
+    case 16: return launch_count_staged<16>(p, c, stream);
     default: break;
   }
   switch (p.seg) {
