@@ -190,32 +190,104 @@ def device_uuid(dev):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_chain_seconds(cfg, scores, bias, down, t0: int, n_tok: int) -> float:
-    """Oracle route -> index -> finalize over tokens [t0, t0+n_tok); returns seconds."""
+def host_threads() -> int:
+    """Host threads this process may run on (std::thread::hardware_concurrency
+    counts the same logical CPUs unless an affinity mask narrows them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (``model name`` in /proc/cpuinfo; on Arm
+    hosts, which do not list one there, lscpu's ``Model name``)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _ranges(n: int, parts: int):
+    return [(n * i // parts, n * (i + 1) // parts) for i in range(parts) if n * i // parts < n * (i + 1) // parts]
+
+
+def oracle_chain_seconds(cfg, scores, bias, down, t0: int, n_tok: int, pool=None,
+                         threads: int = 1) -> float:
+    """Oracle route -> index -> finalize over tokens [t0, t0+n_tok); returns seconds.
+
+    With a thread pool, route and finalize run on `threads` contiguous token
+    ranges at once (each range is an independent oracle call; the oracle
+    releases the interpreter lock while it runs); the index build stays one
+    sequential call, since its stability comes from one ordered walk."""
+    import numpy as np
+
     import oracle
     s = scores[t0:t0 + n_tok]
-    start = time.perf_counter()
-    ids, w = oracle.route(s, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
-    idx = oracle.create_indices(ids, cfg.E)
     N = n_tok * cfg.K
-    oracle.finalize(down[:N], idx["restore_token_order"], w, n_tok, cfg.K, cfg.H)
+    start = time.perf_counter()
+    if pool is None or threads <= 1:
+        ids, w = oracle.route(s, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+        idx = oracle.create_indices(ids, cfg.E)
+        oracle.finalize(down[:N], idx["restore_token_order"], w, n_tok, cfg.K, cfg.H)
+        return time.perf_counter() - start
+    parts = _ranges(n_tok, threads)
+    routed = [pool.submit(oracle.route, s[a:b], bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
+                          cfg.scale) for a, b in parts]
+    res = [f.result() for f in routed]
+    ids = np.concatenate([r[0] for r in res])
+    w = np.concatenate([r[1] for r in res])
+    idx = oracle.create_indices(ids, cfg.E)
+    restore = idx["restore_token_order"]
+    fin = [pool.submit(oracle.finalize, down[:N], restore, w, n_tok, cfg.K, cfg.H,
+                       np.arange(a, b, dtype=np.int64)) for a, b in parts]
+    for f in fin:
+        f.result()
     return time.perf_counter() - start
 
 
-def cpu_baseline(cfg, scores, bias, down, target_s: float):
-    """The oracle as it stands (single thread) on a bounded sample of the workload."""
-    probe_tok = min(cfg.T, 256)
-    probe = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok)
+def _timed_sample(cfg, scores, bias, down, target_s, pool, threads):
+    probe_tok = min(cfg.T, max(256, 64 * threads))
+    probe = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok, pool, threads)
     per_tok = max(probe / probe_tok, 1e-9)
-    n_tok = int(min(cfg.T, max(1, target_s / per_tok)))
+    n_tok = int(min(cfg.T, max(1, target_s / 2 / per_tok)))
+    oracle_chain_seconds(cfg, scores, bias, down, 0, n_tok, pool, threads)  # warm-up pass
     reps, total, done = 0, 0.0, 0
-    while total < target_s and reps < 8:
-        total += oracle_chain_seconds(cfg, scores, bias, down, 0, n_tok)
+    while total < target_s and reps < 64:
+        total += oracle_chain_seconds(cfg, scores, bias, down, 0, n_tok, pool, threads)
         done += n_tok
         reps += 1
-    return {"value": done / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{cfg.name}: tokens 0..{n_tok - 1} of {cfg.T}, route+index+finalize, "
-                      f"{reps} pass(es), {total:.1f} s single-threaded"}
+    return done / total, n_tok, reps, total
+
+
+def cpu_baseline(cfg, scores, bias, down, target_s: float):
+    """The oracle as it stands on a bounded sample of the workload: single
+    thread, and over every host thread (token ranges for route and finalize,
+    the index build sequential). `value` and `cores` are the all-threads run."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = host_threads()
+    v1, n1, r1, s1 = _timed_sample(cfg, scores, bias, down, target_s / 2, None, 1)
+    with ThreadPoolExecutor(threads) as pool:
+        vn, nn, rn, sn = _timed_sample(cfg, scores, bias, down, target_s / 2, pool, threads)
+    return {"value": vn, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{cfg.name}: tokens 0..{nn - 1} of {cfg.T}, route+index+finalize, "
+                      f"{rn} pass(es), {sn:.1f} s on {threads} threads (route and finalize "
+                      f"split by token range, index build sequential)",
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"tokens 0..{n1 - 1}, {r1} pass(es), {s1:.1f} s"},
+            "hardware_concurrency": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def host_inputs(cfg, seed_offset=0, pinned=False):
@@ -236,29 +308,37 @@ def host_inputs(cfg, seed_offset=0, pinned=False):
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return
+    from concurrent.futures import ThreadPoolExecutor
     scores, bias, _, down = host_inputs(cfg)
-    probe_tok = min(cfg.T, 256)
-    per_tok = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok) / probe_tok
-    budget = 150.0  # seconds for warmup + timed steps
-    n_tok = int(max(1, min(cfg.T, budget / max(1, args.steps + args.warmup) / max(per_tok, 1e-9))))
-    t0 = 0
-    for _ in range(args.warmup):
-        oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok)
-        t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
-    total = 0.0
-    for _ in range(args.steps):
-        total += oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok)
-        t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
+    threads = host_threads()
+    with ThreadPoolExecutor(threads) as pool:
+        probe_tok = min(cfg.T, max(256, 64 * threads))
+        per_tok = oracle_chain_seconds(cfg, scores, bias, down, 0, probe_tok, pool,
+                                       threads) / probe_tok
+        budget = 150.0  # seconds for warmup + timed steps
+        n_tok = int(max(1, min(cfg.T, budget / max(1, args.steps + args.warmup)
+                               / max(per_tok, 1e-9))))
+        t0 = 0
+        for _ in range(args.warmup):
+            oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok, pool, threads)
+            t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
+        total = 0.0
+        for _ in range(args.steps):
+            total += oracle_chain_seconds(cfg, scores, bias, down, t0, n_tok, pool, threads)
+            t0 = (t0 + n_tok) % max(1, cfg.T - n_tok + 1)
     value = n_tok * args.steps / total
-    sample = f"{cfg.name}: {n_tok} of {cfg.T} tokens per step, route+index+finalize, single thread"
+    sample = (f"{cfg.name}: {n_tok} of {cfg.T} tokens per step, route+index+finalize on "
+              f"{threads} threads (route and finalize split by token range, index build "
+              f"sequential)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
         "config": config_dict(cfg),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample, "hardware_concurrency": os.cpu_count(),
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
