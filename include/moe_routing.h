@@ -24,8 +24,9 @@
  *   - Argument errors are detected on the host before anything is enqueued
  *     and reported as a moe_status_t. MOE_ERR_CUDA means a launch failed
  *     (cudaGetLastError after the launch). Errors found in the DATA (an
- *     expert id outside [0, n_experts)) are recorded in a device status word
- *     and never trap; see moe_read_device_status.
+ *     expert id outside [0, n_experts), a restore_order entry outside
+ *     [0, T*K)) are recorded in a device status word and never trap; see
+ *     moe_read_device_status.
  *   - A call with zero tokens / slots is valid.
  */
 #ifndef MOE_ROUTING_H
@@ -53,13 +54,16 @@ typedef enum {
   MOE_ERR_MISALIGNED = 3,   /* a pointer breaks the stated alignment */
   MOE_ERR_UNSUPPORTED = 4,  /* valid for the method but outside this library's limits */
   MOE_ERR_CUDA = 5,         /* a CUDA launch or copy failed */
-  MOE_ERR_WORKSPACE = 6     /* workspace NULL or smaller than the size query returns */
+  MOE_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than the size query returns */
+  MOE_ERR_DEVICE_DATA = 7   /* moe_read_device_status: the device status word is not 0 */
 } moe_status_t;
 
-/* Bits of the device status word written by moe_create_indices and moe_route_index. */
+/* Bits of the device status word written by moe_create_indices, moe_route_index
+ * and (when given a status pointer) moe_finalize_ex and moe_permute. */
 #define MOE_DEVICE_STATUS_BAD_EXPERT_ID 0x1u /* some topk_ids entry was outside [0, E) */
 #define MOE_DEVICE_STATUS_SYNC_TIMEOUT 0x2u  /* single-launch route+index: a cross-CTA wait gave up */
 #define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* single-launch route+index: inconsistent counts */
+#define MOE_DEVICE_STATUS_BAD_RESTORE_ORDER 0x8u /* finalize/permute: an entry >= T*K */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024       /* n_routed_experts / n_experts */
@@ -265,7 +269,10 @@ size_t moe_route_index_single_launch_workspace_size(int64_t num_tokens,
  *   the next one.
  *   The CTAs of a call exchange their counts through words tagged with that
  *   call's number, so nothing needs clearing between calls. Calls sharing one
- *   workspace must not overlap.
+ *   workspace must not overlap. The call number is 32 bits wide (after
+ *   0xFFFFFFFF it continues at 2): zero-fill the workspace again at least
+ *   once every 2^31 calls, so that no word left by a call 2^32 calls earlier
+ *   can carry a current number.
  * Execution: one cooperative launch (all CTAs resident at once; CTAs of up
  *   to 1024 threads, at most one per 8 tokens). Every cross-CTA wait gives up
  *   after one second; the call then sets MOE_DEVICE_STATUS_SYNC_TIMEOUT and
@@ -301,7 +308,8 @@ moe_status_t moe_route_index_single_launch(
  * Requirements: T >= 0; 1 <= K <= MOE_MAX_EXPERTS_PER_TOK; T*K < 2^32; H >= 0
  * and H % 8 == 0; output and down 16-byte aligned; restore_order and
  * router_weight 4-byte aligned; output must not overlap down. A
- * restore_order entry >= T*K is skipped (contributes nothing) and never read.
+ * restore_order entry >= T*K is skipped (contributes nothing) and never read;
+ * moe_finalize_ex can also report it.
  */
 moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
                           const uint32_t* restore_order, const float* router_weight,
@@ -320,11 +328,17 @@ moe_status_t moe_finalize(moe_bf16_t* output, const moe_bf16_t* down,
  * output [T, H] of output_dtype, 16-byte aligned. router_weight [T, K] of
  * weight_dtype, aligned to its element size. Other arguments and rules as in
  * moe_finalize; an unknown dtype returns MOE_ERR_UNSUPPORTED.
+ * device_status: optional device pointer (4-byte aligned, or NULL). When
+ *   given, a restore_order entry >= T*K, which is skipped as in moe_finalize,
+ *   also ORs MOE_DEVICE_STATUS_BAD_RESTORE_ORDER into *device_status (never a
+ *   fault or a trap). The word is not cleared by the call: zero it first, and
+ *   read it with moe_read_device_status.
  */
 moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype, const moe_bf16_t* down,
                              const uint32_t* restore_order, const void* router_weight,
                              moe_dtype_t weight_dtype, int64_t num_tokens,
-                             int32_t num_experts_per_token, int64_t hidden, cudaStream_t stream);
+                             int32_t num_experts_per_token, int64_t hidden,
+                             uint32_t* device_status, cudaStream_t stream);
 
 /*
  * moe_permute -- expert-contiguous copy of the token rows, the input of the
@@ -340,16 +354,23 @@ moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype, const moe_b
  * [T*K] uint32 in (as written by moe_create_indices).
  * Requirements: T >= 0; 1 <= K <= MOE_MAX_EXPERTS_PER_TOK; T*K < 2^32; H >= 0
  * and H % 8 == 0; permuted and input 16-byte aligned and not overlapping;
- * restore_token_order 4-byte aligned. An entry >= T*K is skipped.
+ * restore_token_order 4-byte aligned. An entry >= T*K is skipped; with a
+ * device_status pointer (optional, 4-byte aligned, or NULL) it also ORs
+ * MOE_DEVICE_STATUS_BAD_RESTORE_ORDER into *device_status, as moe_finalize_ex.
  */
 moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* input,
                          const uint32_t* restore_token_order, int64_t num_tokens,
-                         int32_t num_experts_per_token, int64_t hidden, cudaStream_t stream);
+                         int32_t num_experts_per_token, int64_t hidden, uint32_t* device_status,
+                         cudaStream_t stream);
 
 /*
- * Reads the device status word that the last moe_create_indices or
- * moe_route_index call on `workspace` wrote (0 = clean; MOE_DEVICE_STATUS_* bits otherwise). Enqueues
- * a 4-byte copy on `stream` and waits for the stream to finish.
+ * Reads a device status word: word 0 of the workspace that the last
+ * moe_create_indices or moe_route_index call on it wrote, or a status word
+ * given to moe_create_indices_no_alloc, moe_finalize_ex or moe_permute
+ * (0 = clean; MOE_DEVICE_STATUS_* bits otherwise). Enqueues a 4-byte copy on
+ * `stream` and waits for the stream to finish. Writes the word to
+ * *host_status and returns MOE_OK when it is 0, MOE_ERR_DEVICE_DATA when it
+ * is not.
  */
 moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status,
                                     cudaStream_t stream);
@@ -375,12 +396,16 @@ moe_status_t moe_read_device_status(const void* workspace, uint32_t* host_status
  * Limits: the scratch that moe_create_indices_workspace_size(num_slots,
  *   n_experts) reports must fit in MOE_NO_ALLOC_SCRATCH_BYTES; a larger
  *   request returns MOE_ERR_WORKSPACE before anything is enqueued. With 1 MiB
- *   this covers, for example, 2 million slots over 128 experts or 1 million
- *   slots over 256 experts.
+ *   the largest accepted num_slots is 2,076,672 over 128 experts, 1,040,384
+ *   over 256 experts and 258,048 over 1024 experts (2^20 slots over 256
+ *   experts need 1,053,952 bytes and are refused).
  * Allocation: the call makes no cudaMalloc, cudaFree or other allocating
  *   call. The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) and caches it, so make that first call before
- *   any stream capture begins.
+ *   any stream capture begins. The cached address is not looked up again:
+ *   do not reset the device (cudaDeviceReset) or otherwise destroy and
+ *   recreate its primary context while the process still calls this entry
+ *   point.
  * Sharing: all calls on a device use the same array. Calls whose work
  *   overlaps on the GPU (different streams, no ordering between them) race on
  *   it and give wrong results. Calls ordered one after another are safe.

@@ -3,9 +3,10 @@
 route (group-limited top-k router) -> create_indices (stable bucket sort by
 expert) -> finalize (fused unpermute + weighted top-k sum), each a CUDA
 kernel behind the C ABI of libmoe_routing.so (include/moe_routing.h);
-route_index runs the first two as one cooperative launch.
+route_index runs the first two together (the router counts its own output).
 """
-from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_SYNC_STATE,
+from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_BAD_RESTORE_ORDER,
+                      DEVICE_STATUS_SYNC_STATE,
                       DEVICE_STATUS_SYNC_TIMEOUT, EXPORTED_SYMBOLS, SCORES_AS_GIVEN,
                       SCORES_SIGMOID, SCORES_SOFTMAX, IndexBuffers, MoeError, MoeLibraryMissing,
                       RouteIndexBuffers, create_indices, finalize, load_library,
@@ -17,7 +18,8 @@ from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_SYNC_STATE,
 from .pipeline import HostStreamer, RoutingPipeline
 
 __all__ = [
-    "DEVICE_STATUS_BAD_EXPERT_ID", "DEVICE_STATUS_SYNC_STATE", "DEVICE_STATUS_SYNC_TIMEOUT",
+    "DEVICE_STATUS_BAD_EXPERT_ID", "DEVICE_STATUS_BAD_RESTORE_ORDER", "DEVICE_STATUS_SYNC_STATE",
+    "DEVICE_STATUS_SYNC_TIMEOUT",
     "EXPORTED_SYMBOLS", "RouteIndexBuffers", "moe_route_index", "moe_route_index_workspace_size",
     "moe_route_index_single_launch_workspace_size", "route_index", "HostStreamer", "IndexBuffers", "MoeError",
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",

@@ -20,10 +20,12 @@ from .build import LIB_PATH
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL_PTR", 2: "MOE_ERR_INVALID_ARG",
                 3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_UNSUPPORTED", 5: "MOE_ERR_CUDA",
-                6: "MOE_ERR_WORKSPACE"}
+                6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_DEVICE_DATA"}
+MOE_ERR_DEVICE_DATA = 7
 DEVICE_STATUS_BAD_EXPERT_ID = 0x1
 DEVICE_STATUS_SYNC_TIMEOUT = 0x2
 DEVICE_STATUS_SYNC_STATE = 0x4
+DEVICE_STATUS_BAD_RESTORE_ORDER = 0x8
 
 # Entry points declared in include/moe_routing.h.
 EXPORTED_SYMBOLS = ("moe_status_string", "moe_route", "moe_create_indices_workspace_size",
@@ -70,9 +72,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_finalize.restype = ctypes.c_int
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_read_device_status.restype = ctypes.c_int
-    lib.moe_permute.argtypes = [vp, vp, vp, i64, i32, i64, vp]
+    lib.moe_permute.argtypes = [vp, vp, vp, i64, i32, i64, vp, vp]
     lib.moe_permute.restype = ctypes.c_int
-    lib.moe_finalize_ex.argtypes = [vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, i64, i32, i64, vp]
+    lib.moe_finalize_ex.argtypes = [vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, i64, i32, i64, vp,
+                                    vp]
     lib.moe_finalize_ex.restype = ctypes.c_int
     lib.moe_route_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, ctypes.c_int,
                                  vp]
@@ -241,8 +244,10 @@ def moe_finalize(output: torch.Tensor, down: torch.Tensor, restore_order: torch.
 
 
 def moe_permute(permuted: torch.Tensor, input: torch.Tensor, restore_token_order: torch.Tensor,
-                stream=None) -> None:
-    """permuted[restore_token_order[t*K+k]] = input[t]: the expert-contiguous token rows."""
+                stream=None, device_status: torch.Tensor | None = None) -> None:
+    """permuted[restore_token_order[t*K+k]] = input[t]: the expert-contiguous token rows.
+    device_status (optional int32 [1] on the device) receives
+    DEVICE_STATUS_BAD_RESTORE_ORDER when an entry is >= T*K (skipped)."""
     T, H = input.shape
     N = restore_token_order.numel()
     K = N // T if T else 1
@@ -251,16 +256,20 @@ def moe_permute(permuted: torch.Tensor, input: torch.Tensor, restore_token_order
     args = (_dev(permuted, "permuted", torch.bfloat16, (N, H)),
             _dev(input, "input", torch.bfloat16),
             _dev(restore_token_order, "restore_token_order", torch.int32, (N,)))
-    _check("moe_permute", load_library().moe_permute(*args, T, K, H, _stream(stream)))
+    st = None if device_status is None else _dev(device_status, "device_status", torch.int32, (1,))
+    _check("moe_permute", load_library().moe_permute(*args, T, K, H, st, _stream(stream)))
 
 
 _DTYPE_CODES = {torch.bfloat16: 0, torch.float32: 1}
 
 
 def moe_finalize_ex(output: torch.Tensor, down: torch.Tensor, restore_order: torch.Tensor,
-                    router_weight: torch.Tensor, stream=None) -> None:
+                    router_weight: torch.Tensor, stream=None,
+                    device_status: torch.Tensor | None = None) -> None:
     """moe_finalize with bf16 or fp32 router weights and a bf16 or fp32 output
-    (taken from the tensors' dtypes)."""
+    (taken from the tensors' dtypes). device_status (optional int32 [1] on the
+    device) receives DEVICE_STATUS_BAD_RESTORE_ORDER when a restore_order entry
+    is >= T*K (skipped)."""
     T, K = router_weight.shape
     H = down.shape[1]
     if output.dtype not in _DTYPE_CODES or router_weight.dtype not in _DTYPE_CODES:
@@ -270,15 +279,19 @@ def moe_finalize_ex(output: torch.Tensor, down: torch.Tensor, restore_order: tor
             _dev(restore_order, "restore_order", torch.int32, (T * K,)),
             _dev(router_weight, "router_weight", router_weight.dtype, (T, K)),
             _DTYPE_CODES[router_weight.dtype])
-    _check("moe_finalize_ex", load_library().moe_finalize_ex(*args, T, K, H, _stream(stream)))
+    st = None if device_status is None else _dev(device_status, "device_status", torch.int32, (1,))
+    _check("moe_finalize_ex", load_library().moe_finalize_ex(*args, T, K, H, st, _stream(stream)))
 
 
 def moe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
-    """Device status word of the last moe_create_indices on this workspace (synchronises)."""
+    """The device status word at the start of `workspace` (an index workspace, or
+    a status word given to another call); synchronises. Returns the word: 0 is
+    clean, otherwise DEVICE_STATUS_* bits."""
     out = ctypes.c_uint32(0)
-    rc = load_library().moe_read_device_status(_dev(workspace, "workspace", torch.uint8),
+    rc = load_library().moe_read_device_status(_dev(workspace, "workspace", workspace.dtype),
                                                ctypes.byref(out), _stream(stream))
-    _check("moe_read_device_status", rc)
+    if rc != MOE_ERR_DEVICE_DATA:
+        _check("moe_read_device_status", rc)
     return int(out.value)
 
 

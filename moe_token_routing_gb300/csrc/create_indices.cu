@@ -95,10 +95,8 @@ moe_status_t launch_index(const IdxArgs& a, const Layout& L, cudaStream_t stream
   const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * a.E;
   if (scatter_smem > 40 * 1024) {  // large E: opt in above the default 48 KB block limit
     const int bytes = (int)scatter_smem;
-    if (cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
-        cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromCounts>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    if (set_dynamic_smem((const void*)idx_scatter_kernel<kBasesSingleCta>, bytes) != MOE_OK ||
+        set_dynamic_smem((const void*)idx_scatter_kernel<kBasesFromCounts>, bytes) != MOE_OK)
       return MOE_ERR_CUDA;
   }
   if (L.num_blocks <= 1) {
@@ -176,7 +174,7 @@ extern "C" moe_status_t moe_read_device_status(const void* workspace, uint32_t* 
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_OK;
+  return *host_status == 0u ? MOE_OK : MOE_ERR_DEVICE_DATA;
 }
 
 // ---------------------------------------------------------------- no-allocation variant

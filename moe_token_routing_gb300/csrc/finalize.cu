@@ -31,7 +31,13 @@ struct FinArgs {
   int K;
   int64_t H8;  // hidden / 8
   uint32_t N;  // T * K
+  uint32_t* status;  // optional: MOE_DEVICE_STATUS_BAD_RESTORE_ORDER for an entry >= N
 };
+
+// Records a skipped restore_order entry (one thread of the CTA reports it).
+__device__ __forceinline__ void report_bad_restore(uint32_t* status) {
+  if (status != nullptr) atomicOr(status, MOE_DEVICE_STATUS_BAD_RESTORE_ORDER);
+}
 
 __device__ __forceinline__ uint4 load_stream(const uint4* p) {
   uint4 v;
@@ -87,13 +93,16 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) 
     int64_t row[K];
     float w[K];
     bool ok[K];
+    bool all_ok = true;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const uint32_t r = __ldg(a.restore + t * K + k);
       ok[k] = r < a.N;
+      all_ok = all_ok && ok[k];
       row[k] = (int64_t)(ok[k] ? r : 0u) * a.H8;
       w[k] = load_weight<WT>(a.weight, t * K + k);
     }
+    if (!all_ok && threadIdx.x == 0) report_bad_restore(a.status);
     for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kFinThreads * kChunkUnroll) {
       uint4 v[kChunkUnroll][K];
 #pragma unroll
@@ -130,7 +139,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
       for (int k = 0; k < a.K; ++k) {
         const uint32_t r = __ldg(a.restore + t * a.K + k);
         const float w = load_weight<WT>(a.weight, t * a.K + k);
-        if (r >= a.N) continue;
+        if (r >= a.N) {
+          if (threadIdx.x == 0 && c0 == 0) report_bad_restore(a.status);
+          continue;
+        }
         const uint4* src = a.down + (int64_t)r * a.H8;
         uint4 v[kChunkUnroll];
 #pragma unroll
@@ -211,6 +223,7 @@ moe_status_t check_and_pack(void* output, size_t out_elem, const moe_bf16_t* dow
   a->K = K;
   a->H8 = hidden / 8;
   a->N = (uint32_t)(T * K);
+  a->status = nullptr;
   return MOE_OK;
 }
 
@@ -233,7 +246,8 @@ extern "C" moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype,
                                         const moe_bf16_t* down, const uint32_t* restore_order,
                                         const void* router_weight, moe_dtype_t weight_dtype,
                                         int64_t num_tokens, int32_t num_experts_per_token,
-                                        int64_t hidden, cudaStream_t stream) {
+                                        int64_t hidden, uint32_t* device_status,
+                                        cudaStream_t stream) {
   using namespace moe;
   const bool out_f32 = output_dtype == MOE_DTYPE_F32, w_f32 = weight_dtype == MOE_DTYPE_F32;
   if ((output_dtype != MOE_DTYPE_BF16 && !out_f32) || (weight_dtype != MOE_DTYPE_BF16 && !w_f32))
@@ -243,6 +257,8 @@ extern "C" moe_status_t moe_finalize_ex(void* output, moe_dtype_t output_dtype,
                                          router_weight, w_f32 ? 4 : 2, num_tokens,
                                          num_experts_per_token, hidden, &a);
   if (st != MOE_OK || num_tokens == 0 || hidden == 0) return st;
+  if (!aligned(device_status, 4)) return MOE_ERR_MISALIGNED;
+  a.status = device_status;
   if (w_f32 && !out_f32) return dispatch_default(a, stream);
   if (w_f32 && out_f32) return dispatch_typed<float, float>(a, stream);
   if (!w_f32 && !out_f32) return dispatch_typed<bf16_t, bf16_t>(a, stream);

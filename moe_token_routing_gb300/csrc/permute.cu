@@ -26,6 +26,7 @@ struct PermArgs {
   int K;
   int64_t H8;
   uint32_t N;
+  uint32_t* status;  // optional: MOE_DEVICE_STATUS_BAD_RESTORE_ORDER for an entry >= N
 };
 
 __device__ __forceinline__ uint4 load_once(const uint4* p) {
@@ -44,12 +45,16 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const PermArgs a)
     int64_t dst[K > 0 ? K : 1];
     bool ok[K > 0 ? K : 1];
     if constexpr (K > 0) {
+      bool all_ok = true;
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const uint32_t r = __ldg(a.restore + t * K + k);
         ok[k] = r < a.N;
+        all_ok = all_ok && ok[k];
         dst[k] = (int64_t)(ok[k] ? r : 0u) * a.H8;
       }
+      if (!all_ok && threadIdx.x == 0 && a.status != nullptr)
+        atomicOr(a.status, MOE_DEVICE_STATUS_BAD_RESTORE_ORDER);
     }
     const uint4* src = a.in + t * a.H8;
     for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kPermThreads * kPermUnroll) {
@@ -72,7 +77,11 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const PermArgs a)
       } else {
         for (int k = 0; k < k_count; ++k) {
           const uint32_t r = __ldg(a.restore + t * k_count + k);
-          if (r >= a.N) continue;
+          if (r >= a.N) {
+            if (threadIdx.x == 0 && c0 == 0 && a.status != nullptr)
+              atomicOr(a.status, MOE_DEVICE_STATUS_BAD_RESTORE_ORDER);
+            continue;
+          }
 #pragma unroll
           for (int u = 0; u < kPermUnroll; ++u) {
             const int64_t c = c0 + (int64_t)u * kPermThreads;
@@ -98,7 +107,7 @@ moe_status_t launch_permute(const PermArgs& a, cudaStream_t stream) {
 extern "C" moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* input,
                                     const uint32_t* restore_token_order, int64_t num_tokens,
                                     int32_t num_experts_per_token, int64_t hidden,
-                                    cudaStream_t stream) {
+                                    uint32_t* device_status, cudaStream_t stream) {
   using namespace moe;
   const int64_t T = num_tokens;
   const int K = num_experts_per_token;
@@ -108,7 +117,8 @@ extern "C" moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* inpu
   if (T * (int64_t)K > (int64_t)0xFFFFFFFFu) return MOE_ERR_UNSUPPORTED;
   if (T == 0 || hidden == 0) return MOE_OK;
   if (!permuted || !input || !restore_token_order) return MOE_ERR_NULL_PTR;
-  if (!aligned(permuted, 16) || !aligned(input, 16) || !aligned(restore_token_order, 4))
+  if (!aligned(permuted, 16) || !aligned(input, 16) || !aligned(restore_token_order, 4) ||
+      !aligned(device_status, 4))
     return MOE_ERR_MISALIGNED;
   const uintptr_t o0 = (uintptr_t)permuted, o1 = o0 + (uintptr_t)(T * K * hidden * 2);
   const uintptr_t i0 = (uintptr_t)input, i1 = i0 + (uintptr_t)(T * hidden * 2);
@@ -122,6 +132,7 @@ extern "C" moe_status_t moe_permute(moe_bf16_t* permuted, const moe_bf16_t* inpu
   a.K = K;
   a.H8 = hidden / 8;
   a.N = (uint32_t)(T * K);
+  a.status = device_status;
   switch (K) {
     case 1: return launch_permute<1>(a, stream);
     case 2: return launch_permute<2>(a, stream);

@@ -46,6 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     assert lib.moe_status_string(0) == b"MOE_OK"
     assert lib.moe_status_string(6) == b"MOE_ERR_WORKSPACE"
+    assert lib.moe_status_string(7) == b"MOE_ERR_DEVICE_DATA"
     assert lib.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
 
 
@@ -184,24 +185,26 @@ def test_finalize_host_validation(lib):
 def test_finalize_ex_host_validation(lib):
     f = lib.moe_finalize_ex
     o, d, r, w = FAKE, FAKE + 0x1000000, FAKE + 0x2000000, FAKE + 0x3000000
-    assert f(o, 2, d, r, w, 1, 4, 2, 64, None) == 4       # unknown output dtype
-    assert f(o, 0, d, r, w, 7, 4, 2, 64, None) == 4       # unknown weight dtype
-    assert f(o, 1, d, r, w + 2, 1, 4, 2, 64, None) == 3   # fp32 weights need 4-byte alignment
-    assert f(o, 1, d, r, w + 2, 0, 0, 2, 64, None) == 0   # T = 0
-    assert f(o, 1, o, r, w, 0, 4, 2, 64, None) == 2       # output overlaps down
-    assert f(o + 8, 1, d, r, w, 0, 4, 2, 64, None) == 3
+    assert f(o, 2, d, r, w, 1, 4, 2, 64, None, None) == 4       # unknown output dtype
+    assert f(o, 0, d, r, w, 7, 4, 2, 64, None, None) == 4       # unknown weight dtype
+    assert f(o, 1, d, r, w + 2, 1, 4, 2, 64, None, None) == 3   # fp32 weights need 4-byte alignment
+    assert f(o, 1, d, r, w + 2, 0, 0, 2, 64, None, None) == 0   # T = 0
+    assert f(o, 1, o, r, w, 0, 4, 2, 64, None, None) == 2       # output overlaps down
+    assert f(o + 8, 1, d, r, w, 0, 4, 2, 64, None, None) == 3
+    assert f(o, 1, d, r, w, 0, 4, 2, 64, FAKE + 2, None) == 3   # status word 4-byte aligned
 
 
 def test_permute_host_validation(lib):
     f = lib.moe_permute
     p = (FAKE, FAKE + 0x1000000, FAKE + 0x2000000)
-    assert f(*p, 4, 2, 60, None) == 4          # hidden % 8
-    assert f(*p, 4, 0, 64, None) == 2
-    assert f(*p, 4, 33, 64, None) == 4
-    assert f(None, *p[1:], 4, 2, 64, None) == 1
-    assert f(p[0] + 8, *p[1:], 4, 2, 64, None) == 3
-    assert f(p[0], p[0], p[2], 4, 2, 64, None) == 2   # permuted overlaps input
-    assert f(None, None, None, 0, 2, 64, None) == 0   # T = 0
+    assert f(*p, 4, 2, 60, None, None) == 4          # hidden % 8
+    assert f(*p, 4, 0, 64, None, None) == 2
+    assert f(*p, 4, 33, 64, None, None) == 4
+    assert f(None, *p[1:], 4, 2, 64, None, None) == 1
+    assert f(p[0] + 8, *p[1:], 4, 2, 64, None, None) == 3
+    assert f(p[0], p[0], p[2], 4, 2, 64, None, None) == 2   # permuted overlaps input
+    assert f(None, None, None, 0, 2, 64, None, None) == 0   # T = 0
+    assert f(*p, 4, 2, 64, FAKE + 2, None) == 3           # status word 4-byte aligned
 
 
 def test_device_status_host_validation(lib):

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import synth
+from _guard import check_all, guarded
 from _workloads import (bits_to_f32, f32_to_bf16_bits, finalize_tolerance_ok, workload,
                         workload_down, workload_finalize_ref)
 
@@ -26,8 +27,10 @@ def gpu_finalize(down_bits, restore, w):
     d = to_dev_bf16(down_bits)
     r = torch.from_numpy(np.ascontiguousarray(restore, dtype=np.uint32).view(np.int32)).cuda()
     ww = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
-    out = moe.finalize(d, r, ww)
-    torch.cuda.synchronize()
+    T, K = ww.shape
+    out, g = guarded((T, d.shape[1]), torch.bfloat16, name="output")
+    moe.moe_finalize(out, d, r, ww)
+    check_all([g])
     return out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
@@ -170,3 +173,41 @@ def test_finalize_ex_default_types_match_finalize():
     moe.moe_finalize_ex(b, d, r, wd)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("K", [8, 3])  # the specialised kernel and the any-K kernel
+def test_out_of_range_restore_entry_sets_status(K):
+    """Page moe_finalize, Args restore_order: an entry >= T*K (corrupt index
+    data) is skipped and never read; with a status word moe_finalize_ex
+    records MOE_DEVICE_STATUS_BAD_RESTORE_ORDER instead of faulting or
+    trapping. Every other token's row is the oracle's, bit for bit, and the
+    bad token's row is the oracle's with that term left out."""
+    import moe_token_routing_gb300 as moe
+    T, H = 97, 520
+    down, restore, w = _case(T, K, H, 1000 + K)
+    bad = restore.copy()
+    bad[5 * K + 1] = T * K          # first value past the end
+    bad[(T - 1) * K] = 0xFFFFFFFF   # the largest value
+    d, wd = to_dev_bf16(down), torch.from_numpy(w).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # a clean call leaves the word at zero
+    out, g = guarded((T, H), torch.bfloat16, name="output")
+    moe.moe_finalize_ex(out, d, torch.from_numpy(restore.view(np.int32)).cuda(), wd,
+                        device_status=status)
+    check_all([g])
+    assert moe.moe_read_device_status(status) == 0
+    out, g = guarded((T, H), torch.bfloat16, name="output")
+    moe.moe_finalize_ex(out, d, torch.from_numpy(bad.view(np.int32)).cuda(), wd,
+                        device_status=status)
+    check_all([g])
+    assert moe.moe_read_device_status(status) == moe.DEVICE_STATUS_BAD_RESTORE_ORDER
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    # the reference with the two bad terms dropped: weight 0 on a valid row
+    w_drop = w.copy()
+    w_drop[5, 1] = 0.0
+    w_drop[T - 1, 0] = 0.0
+    ref = oracle.finalize(down, restore, w_drop, T, K, H)
+    assert finalize_tolerance_ok(got, ref).all()
+    good = np.ones(T, bool)
+    good[[5, T - 1]] = False
+    assert np.array_equal(got[good], f32_to_bf16_bits(ref)[good])

@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import synth
+from _guard import check_all, guard_attrs
 from _workloads import workload
 from test_oracle_index import check_index_outputs
 
@@ -20,8 +21,10 @@ KEYS = ("token_expert_order", "expert_start_indices", "restore_token_order", "ex
 def gpu_index(ids, E):
     import moe_token_routing_gb300 as moe
     t = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)).cuda()
-    bufs = moe.create_indices(t, E)
-    torch.cuda.synchronize()
+    bufs = moe.IndexBuffers(t.numel(), E, "cuda")
+    guards = guard_attrs(bufs, KEYS + ("workspace",))
+    bufs.run(t)
+    check_all(guards)
     out = {k: getattr(bufs, k).cpu().numpy() for k in KEYS}
     for k in ("token_expert_order", "expert_start_indices", "restore_token_order",
               "expert_usage_stats"):

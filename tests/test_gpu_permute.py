@@ -7,6 +7,7 @@ import torch
 
 import oracle
 import synth
+from _guard import check_all, guarded
 from _workloads import bits_to_f32, workload
 
 pytestmark = pytest.mark.gpu
@@ -19,8 +20,10 @@ def to_dev_bf16(bits):
 def gpu_permute(x_bits, restore):
     import moe_token_routing_gb300 as moe
     r = torch.from_numpy(np.ascontiguousarray(restore, dtype=np.uint32).view(np.int32)).cuda()
-    out = moe.permute(to_dev_bf16(x_bits), r)
-    torch.cuda.synchronize()
+    x = to_dev_bf16(x_bits)
+    out, g = guarded((r.numel(), x.shape[1]), torch.bfloat16, name="permuted")
+    moe.moe_permute(out, x, r)
+    check_all([g])
     return out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
@@ -76,4 +79,29 @@ def test_out_of_range_entries_skipped_and_errors():
     assert (got[3] == 0).all()
     lib = moe.load_library()
     st = torch.cuda.current_stream().cuda_stream
-    assert lib.moe_permute(out.data_ptr(), out.data_ptr(), r.data_ptr(), T, K, H, st) == 2
+    assert lib.moe_permute(out.data_ptr(), out.data_ptr(), r.data_ptr(), T, K, H, None,
+                           st) == 2
+
+
+@pytest.mark.parametrize("K", [2, 5])  # the specialised kernel and the any-K kernel
+def test_out_of_range_entry_sets_status(K):
+    """An entry >= T*K is skipped (its slot is never written) and, with a
+    status word, sets MOE_DEVICE_STATUS_BAD_RESTORE_ORDER; no fault."""
+    import moe_token_routing_gb300 as moe
+    T, H = 40, 72
+    x = synth.normal_bf16(9, 4, T * H).reshape(T, H)
+    restore = np.random.default_rng(K).permutation(T * K).astype(np.uint32)
+    slot = int(restore[7])
+    restore[7] = np.uint32(T * K + 3)
+    r = torch.from_numpy(restore.view(np.int32)).cuda()
+    out, g = guarded((T * K, H), torch.bfloat16, fill=0.0, name="permuted")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_permute(out, to_dev_bf16(x), r, device_status=status)
+    check_all([g])
+    assert moe.moe_read_device_status(status) == moe.DEVICE_STATUS_BAD_RESTORE_ORDER
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (got[slot] == 0).all()          # the slot the bad entry named stays unwritten
+    written = np.delete(np.arange(T * K), slot)
+    src = np.empty(T * K, np.int64)
+    src[restore[restore < T * K]] = np.nonzero(restore < T * K)[0] // K
+    assert np.array_equal(got[written], x[src[written]])

@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import synth
+from _guard import check_all, guarded
 from _workloads import workload
 
 pytestmark = pytest.mark.gpu
@@ -30,8 +31,11 @@ def gpu_route(scores, bias, K, G, M, norm, scale, scores_offset=0):
         buf[scores_offset:] = s.reshape(-1)
         s = buf[scores_offset:].view(s.shape)
     b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
-    ids, w = moe.route(s, b, K, G, M, norm, scale)
-    torch.cuda.synchronize()
+    T = s.shape[0]
+    ids, gi = guarded((T, K), torch.int32, name="expert_indices")
+    w, gw = guarded((T, K), torch.float32, name="expert_weights")
+    moe.moe_route(ids, w, s, b, G, M, norm, scale)
+    check_all([gi, gw])
     return ids.cpu().numpy(), w.cpu().numpy()
 
 
@@ -220,10 +224,10 @@ def gpu_route_sigmoid(logits, bias, K, G, M, norm, scale):
     s = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
     b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
     T = logits.shape[0]
-    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
-    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ids, gi = guarded((T, K), torch.int32, name="expert_indices")
+    w, gw = guarded((T, K), torch.float32, name="expert_weights")
     moe.moe_route_ex(ids, w, s, b, G, M, norm, scale, moe.SCORES_SIGMOID)
-    torch.cuda.synchronize()
+    check_all([gi, gw])
     return ids.cpu().numpy(), w.cpu().numpy()
 
 
@@ -261,10 +265,10 @@ def gpu_route_softmax(logits, bias, K, G, M, norm, scale):
     s = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
     b = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
     T = logits.shape[0]
-    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
-    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ids, gi = guarded((T, K), torch.int32, name="expert_indices")
+    w, gw = guarded((T, K), torch.float32, name="expert_weights")
     moe.moe_route_ex(ids, w, s, b, G, M, norm, scale, moe.SCORES_SOFTMAX)
-    torch.cuda.synchronize()
+    check_all([gi, gw])
     return ids.cpu().numpy(), w.cpu().numpy()
 
 
