@@ -321,15 +321,16 @@ __device__ void build_index(const FusedArgs& f, uint32_t* s_warp, const uint32_t
   }
 }
 
-// This call's tag: one more than the last finished call's (0 is skipped, so
-// that a zero-filled workspace never looks ready). CTA 0 also zeroes the
-// counter slot of the next call; the previous user of that slot, the call
-// before this one, has finished.
+// This call's tag: one more than the last finished call's. 0 is never a tag,
+// so a zero-filled workspace never looks ready; after 0xFFFFFFFF comes 2, not
+// 1, so consecutive tags keep alternating in parity, which picks their
+// counter slot. CTA 0 also zeroes the counter slot of the next call; the
+// previous user of that slot, the call before this one, has finished.
 __device__ __forceinline__ uint32_t call_tag(const FusedArgs& f) {
   __shared__ uint32_t s_tag;
   if (threadIdx.x == 0) {
     uint32_t t = load_relaxed(f.calls) + 1u;
-    t = t == 0u ? 1u : t;
+    t = t == 0u ? 2u : t;
     s_tag = t;
     if (blockIdx.x == 0) {
       *counter(f.counted, t + 1u) = 0u;
@@ -424,10 +425,7 @@ moe_status_t launch_fused(Kernel k, FusedArgs f, int warps, int64_t tokens_per_c
                           cudaStream_t stream) {
   // above 40 KB of dynamic shared memory, opt in past the default 48 KB limit
   // (the kernels also hold a few hundred bytes of static shared memory)
-  if (smem > 40 * 1024 &&
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (smem > 40 * 1024 && set_dynamic_smem((const void*)k, smem) != MOE_OK) return MOE_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, warps * 32, smem) !=
           cudaSuccess ||
@@ -614,10 +612,7 @@ template <typename Kernel, typename Args>
 moe_status_t launch_counting_router(Kernel k, const Args& args, int64_t T, int64_t tokens_per_cta,
                                     size_t smem, cudaStream_t stream,
                                     int threads = kRouteThreads) {
-  if (smem > 40 * 1024 &&
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (smem > 40 * 1024 && set_dynamic_smem((const void*)k, smem) != MOE_OK) return MOE_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess ||
       per_sm < 1)
@@ -725,9 +720,7 @@ moe_status_t launch_counting_route(const RoutePlan& p, const CountRouteArgs& c,
 moe_status_t launch_rows_scatter(const IdxArgs& a, cudaStream_t stream) {
   const size_t scatter_smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * a.E;
   if (scatter_smem > 40 * 1024 &&
-      cudaFuncSetAttribute(idx_scatter_kernel<kBasesFromCounts>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)scatter_smem) != cudaSuccess)
+      set_dynamic_smem((const void*)idx_scatter_kernel<kBasesFromCounts>, scatter_smem) != MOE_OK)
     return MOE_ERR_CUDA;
   const moe_status_t st = launch(idx_rows_kernel, (a.E + kRowsWarps - 1) / kRowsWarps,
                                  kRowsWarps * 32, 0, stream, a);
@@ -903,8 +896,7 @@ extern "C" moe_status_t moe_route_index(
   // one CTA places every slot (and writes the status word) without counts
   const size_t smem = sizeof(uint32_t) * (size_t)(kIdxWarps + 5) * x.E;
   if (smem > 40 * 1024 &&
-      cudaFuncSetAttribute(idx_scatter_kernel<kBasesSingleCta>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      set_dynamic_smem((const void*)idx_scatter_kernel<kBasesSingleCta>, smem) != MOE_OK)
     return MOE_ERR_CUDA;
   return launch(idx_scatter_kernel<kBasesSingleCta>, 1, kIdxThreads, smem, stream, x);
 }

@@ -15,6 +15,7 @@ import torch
 
 import oracle
 import synth
+from _guard import check_all, guard_attrs, guarded
 from _workloads import workload
 
 pytestmark = pytest.mark.gpu
@@ -37,9 +38,12 @@ def gpu_route_index(scores, bias, K, G, M, norm, scale, score_fn=0, scales=False
     T, E = scores.shape
     if bufs is None:
         bufs = moe.RouteIndexBuffers(T, E, K, "cuda", single_launch=single)
+    if not hasattr(bufs, "_guards"):
+        bufs._guards = guard_attrs(bufs, ("expert_indices", "expert_weights") + INDEX_KEYS
+                                   + ("workspace",))
     so = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda") if scales else None
     bufs.run(s, b, G, M, norm, scale, score_fn, scales_offset=so)
-    torch.cuda.synchronize()
+    check_all(bufs._guards)
     out = {k: getattr(bufs, k).cpu().numpy() for k in INDEX_KEYS}
     for k in INDEX_KEYS:
         if k != "expert_ids":
@@ -201,11 +205,12 @@ def test_workspace_reused_across_shapes(single):
     big = synth.get_config("dsv3_prefill")
     nbytes = (moe.moe_route_index_single_launch_workspace_size(big.T, big.E) if single
               else moe.moe_route_index_workspace_size(big.T, big.E, big.K))
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    ws, gws = guarded((nbytes,), torch.uint8, fill=0, name="workspace")
     for name in ("dsv3_prefill", "dsv3_decode", "tiny", "skewed_ungrouped", "dsv3_prefill"):
         cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
         bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda", single_launch=single)
-        bufs.workspace = ws
+        bufs.workspace = ws  # the same (guarded) workspace for every call
+        bufs._guards = guard_attrs(bufs, ("expert_indices", "expert_weights") + INDEX_KEYS) + [gws]
         got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights,
                                     cfg.scale, bufs=bufs)
         assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
@@ -213,16 +218,28 @@ def test_workspace_reused_across_shapes(single):
 
 
 def test_call_counter_wraps_past_zero():
-    """Call number 0 is skipped, so a zero-filled word never looks current."""
+    """After call number 0xFFFFFFFF the next is 2: 0 is never a number (a
+    zero-filled word never looks current) and the parity of consecutive
+    numbers, which picks the progress-counter slot, keeps alternating. The
+    workspace is left as call 0xFFFFFFFF would leave it: its counter slot
+    (odd) still holds its final counts, the other slot zeroed."""
     moe = _moe()
     cfg, scores, bias, ids_ref, w_ref, idx_ref = workload("skewed_ungrouped")
     bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda", single_launch=True)
-    bufs.workspace[:8].view(torch.int32)[1] = -1
+    words = bufs.workspace.view(torch.int32)
+    words[1] = -1                    # the last call's number: 0xFFFFFFFF
+    words[(256 + 256) // 4] = 0x7fff  # CTAs-counted slot 1: that call's count
+    words[(768 + 256) // 4] = 0x7fff  # rows-scanned slot 1: that call's count
     got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
                                 bufs=bufs)
     assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
     assert bufs.device_status() == 0
-    assert bufs.workspace[:8].view(torch.int32)[1].item() == 1
+    assert bufs.workspace.view(torch.int32)[1].item() == 2
+    # the next call (number 3, odd) uses slot 1, which call 2 zeroed
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                                bufs=bufs)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+    assert bufs.workspace.view(torch.int32)[1].item() == 3
 
 
 def _selftest_lib():
