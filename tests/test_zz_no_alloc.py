@@ -5,13 +5,19 @@ the library instead of a caller-provided workspace.
 
 Checked through the C ABI against moe_create_indices on two calls in a row
 with different sizes, so that the second call also shows that what the
-first one left in the shared scratch does not leak into its result.
+first one left in the shared scratch does not leak into its result; against
+the CPU oracle element by element (the prefill workload's router output, a
+single-CTA case and the largest request the 1 MiB scratch accepts); and for
+the first request it refuses.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle
+from _guard import check_all, guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -29,17 +35,20 @@ def _lib():
 
 
 def _outputs(N, E):
-    z = dict(dtype=torch.int32, device="cuda")
-    return [torch.full((N,), -5, **z), torch.full((E + 1,), -5, **z), torch.full((N,), -5, **z),
-            torch.full((E,), -5, **z), torch.full((2,), -5, **z)]
+    shapes = ((N,), (E + 1,), (N,), (E,), (2,))
+    names = ("token_expert_order", "expert_start_indices", "restore_token_order", "expert_ids",
+             "expert_usage_stats")
+    pairs = [guarded(sh, torch.int32, fill=-5, name=n) for sh, n in zip(shapes, names)]
+    return [p[0] for p in pairs], [p[1] for p in pairs]
 
 
 def _no_alloc(lib, ids, E, status):
-    outs = _outputs(ids.numel(), E)
+    outs, guards = _outputs(ids.numel(), E)
     rc = lib.moe_create_indices_no_alloc(*[t.data_ptr() for t in outs], ids.data_ptr(),
                                          ids.numel(), E, status.data_ptr(),
                                          torch.cuda.current_stream().cuda_stream)
     assert rc == 0
+    check_all(guards)
     return outs
 
 
@@ -88,3 +97,51 @@ def test_rejects_requests_beyond_the_scratch_size():
     fake = 0x7f0000001000  # never dereferenced: the call fails before enqueueing
     rc = lib.moe_create_indices_no_alloc(fake, fake, fake, fake, fake, fake, N, E, None, None)
     assert rc == 6  # MOE_ERR_WORKSPACE
+
+
+INDEX_KEYS = ("token_expert_order", "expert_start_indices", "restore_token_order", "expert_ids",
+              "expert_usage_stats")
+
+
+def _assert_matches_oracle(got, ids_np, E):
+    ref = oracle.create_indices(ids_np, E)
+    for k, g in zip(INDEX_KEYS, got):
+        r = ref[k]
+        g = g.cpu().numpy()
+        g = g if k == "expert_ids" else g.view(np.uint32)
+        assert np.array_equal(g, r), k
+
+
+@pytest.mark.parametrize("case", ["prefill_router_ids", "single_cta", "largest_accepted"])
+def test_matches_oracle(case):
+    """Element by element against the oracle's bucket sort (page
+    moe_create_indices: every output), twice in a row on the shared scratch."""
+    moe, lib = _lib()
+    status = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    if case == "prefill_router_ids":
+        from _workloads import workload
+        cfg, _, _, ids_ref, _, _ = workload("dsv3_prefill")
+        ids_np, E = ids_ref.reshape(-1).astype(np.int32), cfg.E
+    elif case == "single_cta":
+        ids_np, E = np.random.default_rng(5).integers(0, 16, size=1000).astype(np.int32), 16
+    else:
+        E = 256
+        N = 1_040_384  # the largest num_slots over 256 experts that fits 1 MiB
+        assert moe.moe_create_indices_workspace_size(N, E) <= MAX_SCRATCH
+        assert moe.moe_create_indices_workspace_size(N + 1, E) > MAX_SCRATCH
+        ids_np = np.random.default_rng(6).integers(0, E, size=N).astype(np.int32)
+    ids = torch.from_numpy(ids_np).cuda()
+    for _ in range(2):
+        got = _no_alloc(lib, ids, E, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _assert_matches_oracle(got, ids_np, E)
+
+
+def test_rejects_the_first_request_over_the_limit():
+    moe, lib = _lib()
+    for N, E in ((1_040_385, 256), (1 << 20, 256), (2_076_673, 128)):
+        assert moe.moe_create_indices_workspace_size(N, E) > MAX_SCRATCH
+        fake = 0x7f0000001000  # never dereferenced: the call fails before enqueueing
+        rc = lib.moe_create_indices_no_alloc(fake, fake, fake, fake, fake, fake, N, E, None, None)
+        assert rc == 6  # MOE_ERR_WORKSPACE
