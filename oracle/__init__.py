@@ -50,11 +50,13 @@ def _open(path: str):
     lib.oracle_finalize_f64.argtypes = [vp, vp, vp, i64, i32, i64, vp]
     lib.oracle_permute.argtypes = [vp, vp, i64, i32, i64, vp]
     lib.oracle_scales_offsets.argtypes = [vp, i64, i32, ctypes.c_uint32, vp]
+    lib.oracle_exp.argtypes = [vp, i64, vp]
     lib.oracle_sigmoid.argtypes = [vp, i64, vp]
     lib.oracle_softmax.argtypes = [vp, i64, i32, vp]
     for f in (lib.oracle_route, lib.oracle_create_indices, lib.oracle_finalize,
               lib.oracle_finalize_tokens, lib.oracle_finalize_f64, lib.oracle_permute,
-              lib.oracle_scales_offsets, lib.oracle_sigmoid, lib.oracle_softmax):
+              lib.oracle_scales_offsets, lib.oracle_exp, lib.oracle_sigmoid,
+              lib.oracle_softmax):
         f.restype = ctypes.c_int
     return lib
 
@@ -172,6 +174,14 @@ def scales_offsets(topk_ids, E: int, row_align: int = 128):
     out = np.empty(E + 1, dtype=np.uint32)
     rc = _load().oracle_scales_offsets(ip, ids.size, E, row_align, out.ctypes.data)
     _check(rc, "oracle_scales_offsets")
+    return out
+
+
+def exp_f32(x):
+    """fp32 exp of the score loaders (argument clamped to [-87, 88])."""
+    a, ap = _c(x, np.float32)
+    out = np.empty_like(a)
+    _check(_load().oracle_exp(ap, a.size, out.ctypes.data), "oracle_exp")
     return out
 
 

@@ -40,6 +40,17 @@ float exp_cody_waite(float x) {
 
 }  // namespace
 
+// The exp that both score loaders below use, one value per element (its
+// own pin compares it with a double-precision exp).
+extern "C" int oracle_exp(const float* x, int64_t n, float* out) {
+  if (n < 0) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (std::isnan(x[i])) return ORACLE_ERR_NAN;
+    out[i] = exp_cody_waite(x[i]);
+  }
+  return ORACLE_OK;
+}
+
 // group_limited_router_kernel, Parameters scores_input_fn: an optional loader
 // of each (token, expert) score; here the score of a gate logit x is its
 // sigmoid 1 / (1 + exp(-x)).

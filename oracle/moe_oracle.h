@@ -58,8 +58,13 @@ extern "C" {
 #define ORACLE_ERR_NAN -2
 #define ORACLE_ERR_DATA -3
 
-/* Sigmoid score loader: out[i] = 1 / (1 + exp(-x[i])) in fp32, with exp by
- * Cody-Waite reduction and a degree-7 Taylor polynomial (see the .cpp). */
+/* The exp of the score loaders, exposed for its own pin: out[i] =
+ * exp(clamp(x[i], -87, 88)) in fp32 by Cody-Waite reduction and a degree-7
+ * Taylor polynomial (see the .cpp). */
+int oracle_exp(const float* x, int64_t n, float* out);
+
+/* Sigmoid score loader: out[i] = 1 / (1 + exp(-x[i])) in fp32, with the exp
+ * of oracle_exp. */
 int oracle_sigmoid(const float* x, int64_t n, float* out);
 
 /* Softmax score loader (Parameters scores_input_fn): out[r, e] =

@@ -15,6 +15,7 @@ import oracle
 import test_oracle_finalize as tf
 import test_oracle_index as ti
 import test_oracle_permute as tp
+import test_oracle_exp as tex
 import test_oracle_route as tr
 import test_oracle_scales as tsc
 import test_oracle_sigmoid as tsg
@@ -68,6 +69,9 @@ MUTANTS = {
                                       "ex[e] = exp_cody_waite(row[e]);"),
     "softmax sum skips the first expert": ("      sum += ex[e];", "      if (e > 0) sum += ex[e];"),
     "softmax max taken as the first logit": ("      if (row[e] > m) m = row[e];", "      (void)m;"),
+    "exp with a wrong 1/5! coefficient": ("8.33333333333333333e-3f,", "8.33333333333333333e-2f,"),
+    "exp rounds n towards zero": ("const float n = std::rint(x * 1.44269504088896341f);",
+                                  "const float n = std::trunc(x * 1.44269504088896341f);"),
     "permute copies the slot's row": ("out[p * H + h] = input[t * H + h];",
                                       "out[p * H + h] = input[(p / K) * H + h];"),
 }
@@ -102,6 +106,8 @@ def _pins():
         tsm.test_large_logits_need_the_max_shift,
         tsm.test_all_equal_row_is_exactly_uniform,
         tsm.test_one_dominant_logit,
+        tex.test_binade_endpoints_within_bound,
+        tex.test_exact_points_and_clamp,
     ]
 
 
