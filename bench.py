@@ -48,11 +48,14 @@ def parse_args():
     p.add_argument("--config", default="dsv3_prefill")
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (profiling runs)")
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--separate-index", action="store_true",
                    help="time moe_route followed by moe_create_indices in the steps "
                         "instead of the fused moe_route_index")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the router back-to-back / large-batch measurements and the "
+                        "secondary workloads (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args()
@@ -355,6 +358,147 @@ def config_dict(cfg):
                   "256 MB read (so no dirty flush lines are written back inside the step)"}
 
 
+
+# ---------------------------------------------------------------- extra measurements
+def router_bytes(T: int, E: int, K: int) -> int:
+    return 4 * T * E + 4 * E + 8 * T * K
+
+
+def time_back_to_back(fn, n: int, stream, host=None) -> float:
+    """Mean device time (us) of n calls of fn(i) launched back to back
+    between one pair of events; `host` (a dict) receives the host time per
+    call spent enqueueing them."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    h0 = time.perf_counter()
+    for i in range(n):
+        fn(i)
+    h1 = time.perf_counter()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if host is not None:
+        host["host_enqueue_us_per_launch"] = (h1 - h0) * 1e6 / n
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
+def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
+    """The router alone, launched back to back: on the workload's batch
+    rotating over copies whose total exceeds L2 twice over, on a 262144-token
+    batch (one 268 MB input, larger than L2), and on 8 tokens (one chunk: the
+    per-launch floor of the same kernel, with next to no data)."""
+    import torch
+
+    import synth
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    T, E, K = cfg.T, cfg.E, cfg.K
+    nbuf = max(2, -(-2 * l2 // (4 * T * E)))
+    bufs = [s_d.clone() for _ in range(nbuf)]
+    n = 48
+
+    lib = moe.load_library()
+    sh = stream.cuda_stream
+
+    def route_fn(src, ids, w):
+        # the C ABI called directly with the pointers taken once, so that the
+        # host enqueues faster than the device runs the launches
+        ptrs = [x.data_ptr() for x in src]
+        Tn = src[0].shape[0]
+        a = (ids.data_ptr(), w.data_ptr())
+
+        def call(i):
+            rc = lib.moe_route(a[0], a[1], ptrs[i % len(ptrs)], b_d.data_ptr(), Tn, E, K, cfg.G,
+                               cfg.M, int(cfg.norm_weights), float(cfg.scale), sh)
+            if rc != 0:
+                raise RuntimeError(f"moe_route failed: {rc}")
+        return call
+
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    f = route_fn(bufs, ids, w)
+    for i in range(3):
+        f(i)
+    hb = {}
+    b2b = time_back_to_back(f, n, stream, hb)
+    del bufs
+    big_T = 262144
+    big = torch.from_numpy(synth.make_scores(cfg.replace(T=big_T))).to(dev)
+    ids_b = torch.empty((big_T, K), dtype=torch.int32, device=dev)
+    w_b = torch.empty((big_T, K), dtype=torch.float32, device=dev)
+    fb = route_fn([big], ids_b, w_b)
+    for i in range(3):
+        fb(i)
+    big_b2b = time_back_to_back(fb, 20, stream)
+    del big, ids_b, w_b
+    small = s_d[:8].contiguous()
+    fs = route_fn([small], ids[:8].contiguous(), w[:8].contiguous())
+    for i in range(3):
+        fs(i)
+    hf = {}
+    floor = time_back_to_back(fs, n, stream, hf)
+    rb = router_bytes(T, E, K)
+    bb = router_bytes(big_T, E, K)
+    return {
+        "back_to_back": dict(hb, **{"launches": n, "us_per_launch": b2b,
+                         "achieved_gbs": rb / (b2b * 1e-6) / 1e9,
+                         "frac": rb / (b2b * 1e-6) / 1e9 / peak,
+                         "inputs": f"{nbuf} copies of the {T}-token score matrix in rotation "
+                                   f"({nbuf * 4 * T * E / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)"}),
+        "large_batch": {"tokens": big_T, "launches": 20, "us_per_launch": big_b2b,
+                        "achieved_gbs": bb / (big_b2b * 1e-6) / 1e9,
+                        "frac": bb / (big_b2b * 1e-6) / 1e9 / peak,
+                        "algorithmic_bytes": bb},
+        "launch_floor": dict(hf, **{"tokens": 8, "launches": n, "us_per_launch": floor,
+                                    "note": "the same router on one 8-token chunk, back to "
+                                            "back"}),
+        "hbm_time_at_peak_us": rb / (peak * 1e3),
+        "residue_over_hbm_time_us": b2b - rb / (peak * 1e3),
+    }
+
+
+def secondary_workload(moe, name, dev, stream, peak, flush_l2, reps=50):
+    """Route + index and finalize stage times of another large workload
+    (separate passes, L2 flushed before each call)."""
+    import statistics
+
+    import torch
+
+    import synth
+    c = synth.get_config(name)
+    scores = torch.from_numpy(synth.make_scores(c)).to(dev)
+    bias = torch.from_numpy(synth.make_bias(c)).to(dev)
+    down = torch.empty((c.N, c.H), dtype=torch.bfloat16)
+    synth.make_down(c, out_ptr=down.data_ptr())
+    down = down.to(dev)
+    pipe = moe.RoutingPipeline(c.T, c.E, c.K, c.H, c.G, c.M, c.norm_weights, c.scale,
+                               device=dev, fused=True)
+    for _ in range(3):
+        pipe(scores, bias, down)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for i in range(reps):
+        flush_l2()
+        ev[i][0].record(stream)
+        pipe.route_and_index(scores, bias)
+        ev[i][1].record(stream)
+        pipe.finalize(down)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    ri = statistics.fmean([e[0].elapsed_time(e[1]) for e in ev])
+    fin = statistics.fmean([e[1].elapsed_time(e[2]) for e in ev])
+    fb = 2 * c.N * c.H + 8 * c.N + 2 * c.T * c.H
+    ok = moe.moe_read_device_status(pipe.fused_workspace) == 0
+    out = {"tokens": c.T, "n_routed_experts": c.E, "n_experts_per_tok": c.K, "hidden": c.H,
+           "route_index_ms": ri, "finalize_ms": fin, "step_ms": ri + fin,
+           "tokens_per_s": c.T / ((ri + fin) * 1e-3),
+           "finalize_gbs": fb / (fin * 1e-3) / 1e9, "finalize_frac": fb / (fin * 1e-3) / 1e9 / peak,
+           "finalize_algorithmic_bytes": fb, "device_status_clean": ok, "reps": reps}
+    del pipe, scores, bias, down
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, cfg, rank, world, local_rank):
     import numpy as np
@@ -520,6 +664,16 @@ def run_gpu(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     soft_ms = statistics.fmean([e[0].elapsed_time(e[1]) for e in pev])
 
+    # ---- the router's own evidence and the other large workloads (rank 0, after
+    # the timed steps)
+    peak_gbs, _ = measured_hbm_peak()
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras["router"] = router_evidence(moe, cfg, s_d, b_d, dev, stream, peak_gbs)
+        for name in ("skewed_ungrouped", "few_expert_large_batch"):
+            if name != cfg.name:
+                extras[name] = secondary_workload(moe, name, dev, stream, peak_gbs, flush_l2)
+
     # ---- end to end through the host-buffer API: pinned inputs copied in and the
     # output copied back every step, copies of consecutive steps overlapped
     s_h = torch.from_numpy(scores).pin_memory()
@@ -577,10 +731,13 @@ def run_gpu(args, cfg, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": nbytes["finalize"],
                      "traffic": profile_traffic("finalize.cu", "finalize_dsv3_prefill.txt")
                      if cfg.name == "dsv3_prefill" else None},
-        "router_roofline": {"bound": "hbm", "achieved": route_gbs, "peak": peak, "unit": "GB/s",
-                            "frac": route_gbs / peak,
-                            "frac_vs_nominal_8tbs": route_gbs / NOMINAL_HBM_GBS,
-                            "algorithmic_bytes_per_launch": nbytes["route"]},
+        "router_roofline": dict({"bound": "hbm", "achieved": route_gbs, "peak": peak,
+                                 "unit": "GB/s", "frac": route_gbs / peak,
+                                 "frac_vs_nominal_8tbs": route_gbs / NOMINAL_HBM_GBS,
+                                 "algorithmic_bytes_per_launch": nbytes["route"],
+                                 "timing": "single launch, L2 flushed, mean of the stage pass"},
+                                **extras.get("router", {})),
+        "secondary_workloads": {k: v for k, v in extras.items() if k != "router"},
         "stages_ms": {"route": route_mean, "create_indices": statistics.fmean(index_ms),
                       "route_index_fused": statistics.fmean(fused_ms),
                       "route_index_single_launch": statistics.fmean(single_ms),

@@ -1,5 +1,6 @@
 // Library-wide pieces of the C ABI: status names and cached device facts.
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -25,6 +26,36 @@ DeviceInfo device_info() {
   return cache[dev];
 }
 
+moe_status_t set_dynamic_smem(const void* kernel, size_t bytes) {
+  struct Entry {
+    const void* kernel;
+    int device;
+    size_t bytes;
+  };
+  constexpr int kMaxEntries = 512;
+  static Entry table[kMaxEntries];
+  static int used = 0;
+  static std::mutex lock;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> guard(lock);
+  int slot = -1;
+  for (int i = 0; i < used; ++i)
+    if (table[i].kernel == kernel && table[i].device == dev) {
+      if (table[i].bytes >= bytes) return MOE_OK;
+      slot = i;
+      break;
+    }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (slot < 0 && used < kMaxEntries) slot = used++;
+  if (slot >= 0) table[slot] = Entry{kernel, dev, bytes};
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" const char* moe_status_string(moe_status_t status) {
@@ -36,6 +67,7 @@ extern "C" const char* moe_status_string(moe_status_t status) {
     case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_DEVICE_DATA: return "MOE_ERR_DEVICE_DATA";
   }
   return "MOE_ERR_UNKNOWN";
 }

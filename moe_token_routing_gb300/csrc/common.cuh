@@ -31,6 +31,12 @@ struct DeviceInfo {
 };
 DeviceInfo device_info();
 
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes`. The largest size set so far is remembered per kernel and
+// device, so repeated launches of the same shape make no further runtime
+// call. Callers skip it below the default limit.
+moe_status_t set_dynamic_smem(const void* kernel, size_t bytes);
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 inline moe_status_t launch_status() {

@@ -75,11 +75,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_thread_kernel(const Route
 template <typename Kernel>
 moe_status_t launch_route(Kernel k, const RouteArgs& a, int64_t tokens_per_cta, size_t smem,
                           cudaStream_t stream, int threads = kRouteThreads) {
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
+  if (smem > 48 * 1024 && set_dynamic_smem((const void*)k, smem) != MOE_OK) return MOE_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess ||
       per_sm < 1)

@@ -683,9 +683,7 @@ template <typename Args>
 moe_status_t launch_staged(void (*kernel)(Args, StagedSplit), const Args& args, int64_t T, int E,
                            int tokens, cudaStream_t stream) {
   const StagedShape q = staged_shape(T, E, tokens, device_info().sm_count);
-  if (q.smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q.smem) !=
-          cudaSuccess)
+  if (q.smem > 48 * 1024 && set_dynamic_smem((const void*)kernel, q.smem) != MOE_OK)
     return MOE_ERR_CUDA;
   const int64_t chunks = (T + tokens - 1) / tokens;
   StagedSplit sp;
