@@ -350,17 +350,29 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     mbar_arrive_expect_tx(&bars[s], bytes);
     bulk_copy_g2s(ring + (size_t)s * kRow, a.scores + t0 * E, bytes, &bars[s]);
   };
-  // the first copies start before the bias is staged
+  // The bias loads go out first (a load issued after the chunk copies waits
+  // behind them at the memory), then lane 0 of each warp starts its first D
+  // chunk copies; the bias reaches shared memory while they are in flight.
+  constexpr int kBiasPer = (E / 4 + 31) / 32;  // float4 loads per thread at W = 1
+  float4 bv[kBiasPer];
+#pragma unroll
+  for (int q = 0; q < kBiasPer; ++q) {
+    const int i = threadIdx.x + q * blockDim.x;
+    if (i < E / 4) bv[q] = __ldg(reinterpret_cast<const float4*>(a.bias) + i);
+  }
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(&bars[s], 1u);
     fence_barrier_init();
     for (int s = 0; s < D && c0 + warp + (int64_t)s * W < c1; ++s) issue(c0 + warp + (int64_t)s * W, s);
   }
   // the bias, a -0 stored as +0 (see stage_seg_bias)
-  for (int i = threadIdx.x; i < E / 4; i += blockDim.x) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(a.bias) + i);
-    reinterpret_cast<float4*>(s_bias)[i] = make_float4(
-        __fadd_rn(v.x, 0.0f), __fadd_rn(v.y, 0.0f), __fadd_rn(v.z, 0.0f), __fadd_rn(v.w, 0.0f));
+#pragma unroll
+  for (int q = 0; q < kBiasPer; ++q) {
+    const int i = threadIdx.x + q * blockDim.x;
+    if (i < E / 4)
+      reinterpret_cast<float4*>(s_bias)[i] =
+          make_float4(__fadd_rn(bv[q].x, 0.0f), __fadd_rn(bv[q].y, 0.0f), __fadd_rn(bv[q].z, 0.0f),
+                      __fadd_rn(bv[q].w, 0.0f));
   }
   __syncthreads();
 
