@@ -20,8 +20,7 @@
  *   - the expert-contiguous token rows that the grouped matmul consumes
  *     ("moe_create_indices", description paragraph).
  *
- * Readings where the pages are silent (each is listed with its reason in the
- * design notes of this repository):
+ * Readings where the pages are silent:
  *   - group score = sum of the group's two largest biased scores (one score if
  *     the group has a single expert);
  *   - ties (groups and experts) go to the lower index, comparing IEEE values;
