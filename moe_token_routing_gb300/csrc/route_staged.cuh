@@ -410,7 +410,8 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     float* row = ring + (size_t)s * kRow + tq * E;
 
     // ---- pass 1: scores of this thread's P groups (top-2 of each float4 by
-    // two min/max pairs, then merged into the running top-2) ----
+    // two min/max pairs, then the eight float4 top-2s merged as a tree, so the
+    // merges of a group form three dependent levels rather than a chain) ----
     uint32_t gk[P];   // order keys of the group scores
     float sec[P];     // second-best biased score of each group
 #pragma unroll
@@ -418,7 +419,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
       const int grp = h * P + i;
       float* rg = row + grp * 32;
       const float* bg = s_bias + grp * 32;
-      float t1 = 0.0f, t2 = 0.0f;
+      float q1[8], q2[8];  // top-2 of each float4
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int col = ((c + rot) & 7) * 4;
@@ -433,18 +434,20 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
         const float z = __fadd_rn(v.z, bb.z), w = __fadd_rn(v.w, bb.w);
         const float hi1 = fmaxf(x, y), lo1 = fminf(x, y);
         const float hi2 = fmaxf(z, w), lo2 = fminf(z, w);
-        const float p1 = fmaxf(hi1, hi2);
-        const float p2 = fmax3(fminf(hi1, hi2), lo1, lo2);
-        if (c == 0) {
-          t1 = p1;
-          t2 = p2;
-        } else {
-          t2 = fmax3(fminf(t1, p1), t2, p2);
-          t1 = fmaxf(t1, p1);
-        }
+        q1[c] = fmaxf(hi1, hi2);
+        q2[c] = fmax3(fminf(hi1, hi2), lo1, lo2);
       }
-      gk[i] = score_order_key(__fadd_rn(t1, t2));
-      sec[i] = t2;
+      // merge (a1, a2) with (b1, b2): the larger first, and the larger of the
+      // smaller first and both seconds
+#pragma unroll
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) {
+          q2[c] = fmax3(fminf(q1[c], q1[c + w]), q2[c], q2[c + w]);
+          q1[c] = fmaxf(q1[c], q1[c + w]);
+        }
+      gk[i] = score_order_key(__fadd_rn(q1[0], q2[0]));
+      sec[i] = q2[0];
     }
     if constexpr (kSigmoid) __syncwarp();
 
