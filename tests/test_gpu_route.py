@@ -305,3 +305,48 @@ def test_softmax_loader_shapes_and_extremes(E, G, M, K, norm):
     ids, w = gpu_route_softmax(logits, bias, K, G, M, norm, 2.5)
     assert np.array_equal(ids, ids_ref)
     assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
+def _mbar_selftest_lib():
+    """The bounded-wait harness of tests/cuda (the staged router's chunk wait),
+    built with nvcc for sm_103a."""
+    import ctypes
+    import os
+    import subprocess
+    from moe_token_routing_gb300 import build
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "cuda", "mbar_wait_selftest.cu")
+    so = os.path.join(here, "cuda", "libmbar_wait_selftest.so")
+    hdr = os.path.join(os.path.dirname(os.path.abspath(build.__file__)), "csrc")
+    deps = [src, os.path.join(hdr, "mbarrier.cuh"), os.path.join(hdr, "tagged_sync.cuh")]
+    if not os.path.exists(so) or any(os.path.getmtime(so) < os.path.getmtime(d) for d in deps):
+        subprocess.run([build.nvcc()] + build.ARCH_FLAGS + ["-O2", "-std=c++17", "-Xcompiler",
+                        "-fPIC", "-shared", "-I", hdr, "-I", os.path.join(build.ROOT, "include"),
+                        src, "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    vp = ctypes.c_void_p
+    lib.mbar_wait_selftest.argtypes = [vp, ctypes.c_int, vp, vp]
+    lib.mbar_wait_selftest.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("complete", [True, False])
+def test_bounded_chunk_wait(complete):
+    """The staged router's wait for a score chunk: when the bulk copy lands the
+    wait returns at once with the data; when nothing arrives (a barrier no copy
+    completes) it gives up after its one-second limit and reports failure, and
+    the GPU stays usable. A router warp that gives up writes id -1 for its
+    tokens, which moe_route_index reports as a bad expert id."""
+    lib = _mbar_selftest_lib()
+    src = torch.tensor([0x1234, 5, 6, 7], dtype=torch.int32, device="cuda")
+    out = torch.full((2,), 7, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = lib.mbar_wait_selftest(src.data_ptr(), int(complete), out.data_ptr(), elapsed.data_ptr())
+    assert rc == 0
+    ok, first = out.cpu().tolist()
+    seconds = elapsed.item() * 1e-9
+    if complete:
+        assert ok == 1 and first == 0x1234 and seconds < 0.5
+    else:
+        assert ok == 0 and 0.9 < seconds < 5.0
+    assert torch.ones(4, device="cuda").sum().item() == 4.0
