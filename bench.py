@@ -384,6 +384,37 @@ def time_back_to_back(fn, n: int, stream, host=None) -> float:
     return e0.elapsed_time(e1) * 1e3 / n
 
 
+def time_graph_replay(fn, n: int, dev, reps: int = 10):
+    """Mean device time (us) per call when n calls of fn(i, stream), captured
+    in a CUDA graph, are replayed `reps` times back to back: no host work per
+    launch. None if the capture fails."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    try:
+        with torch.cuda.stream(s):
+            for i in range(n):
+                fn(i, s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(n):
+                fn(i, s)
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * n)
+
+
 def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     """The router alone, launched back to back: on the workload's batch
     rotating over copies whose total exceeds L2 twice over, on a 262144-token
@@ -401,16 +432,17 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     lib = moe.load_library()
     sh = stream.cuda_stream
 
-    def route_fn(src, ids, w):
+    def route_fn(src, ids, w, on_stream=False):
         # the C ABI called directly with the pointers taken once, so that the
         # host enqueues faster than the device runs the launches
         ptrs = [x.data_ptr() for x in src]
         Tn = src[0].shape[0]
         a = (ids.data_ptr(), w.data_ptr())
 
-        def call(i):
+        def call(i, st=None):
             rc = lib.moe_route(a[0], a[1], ptrs[i % len(ptrs)], b_d.data_ptr(), Tn, E, K, cfg.G,
-                               cfg.M, int(cfg.norm_weights), float(cfg.scale), sh)
+                               cfg.M, int(cfg.norm_weights), float(cfg.scale),
+                               st.cuda_stream if st is not None else sh)
             if rc != 0:
                 raise RuntimeError(f"moe_route failed: {rc}")
         return call
@@ -422,6 +454,7 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
         f(i)
     hb = {}
     b2b = time_back_to_back(f, n, stream, hb)
+    graph_b2b = time_graph_replay(f, n, dev)
     del bufs
     big_T = 262144
     big = torch.from_numpy(synth.make_scores(cfg.replace(T=big_T))).to(dev)
@@ -431,6 +464,7 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     for i in range(3):
         fb(i)
     big_b2b = time_back_to_back(fb, 20, stream)
+    big_graph = time_graph_replay(fb, 20, dev, reps=3)
     del big, ids_b, w_b
     small = s_d[:8].contiguous()
     fs = route_fn([small], ids[:8].contiguous(), w[:8].contiguous())
@@ -438,8 +472,15 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
         fs(i)
     hf = {}
     floor = time_back_to_back(fs, n, stream, hf)
+    floor_graph = time_graph_replay(fs, n, dev)
     rb = router_bytes(T, E, K)
     bb = router_bytes(big_T, E, K)
+
+    def graph_entry(us, nbytes):
+        if us is None:
+            return None
+        return {"us_per_launch": us, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+                "frac": nbytes / (us * 1e-6) / 1e9 / peak}
     return {
         "back_to_back": dict(hb, **{"launches": n, "us_per_launch": b2b,
                          "achieved_gbs": rb / (b2b * 1e-6) / 1e9,
@@ -453,6 +494,12 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
         "launch_floor": dict(hf, **{"tokens": 8, "launches": n, "us_per_launch": floor,
                                     "note": "the same router on one 8-token chunk, back to "
                                             "back"}),
+        "graph_replay": {
+            "note": "the same launches captured in a CUDA graph and replayed: no host work "
+                    "per launch",
+            "back_to_back": graph_entry(graph_b2b, rb),
+            "large_batch": graph_entry(big_graph, bb),
+            "launch_floor_us": floor_graph},
         "hbm_time_at_peak_us": rb / (peak * 1e3),
         "residue_over_hbm_time_us": b2b - rb / (peak * 1e3),
     }
