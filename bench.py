@@ -747,6 +747,21 @@ def run_gpu(args, cfg, rank, world, local_rank):
     streamer.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
     h2d, d2h = pipe.host_bytes()
+    # The host link in the same run: the step's input copies alone, back to
+    # back on the copy-in stream (its throughput moves by about 10% between
+    # runs on this kind of host, so e2e is read against this figure).
+    slot = streamer.slots[0]
+    with torch.cuda.stream(streamer.copy_in):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(streamer.copy_in)
+        for _ in range(5):
+            slot["scores"].copy_(s_h, non_blocking=True)
+            slot["bias"].copy_(b_h, non_blocking=True)
+            slot["down"].copy_(down_h, non_blocking=True)
+        c1.record(streamer.copy_in)
+    streamer.synchronize()
+    h2d_only_ms = c0.elapsed_time(c1) / 5
 
     if rank != 0:
         if world > 1:
@@ -828,7 +843,11 @@ def run_gpu(args, cfg, rank, world, local_rank):
                 "api": "RoutingPipeline.stream_from_host (copies of consecutive steps overlap)",
                 "timing": "steady state: the timed steps follow three untimed ones in stream "
                           "order; events on the copy-in stream at the start and the copy-out "
-                          "stream at the end"},
+                          "stream at the end",
+                "host_link": {"h2d_ms_per_step": h2d_only_ms,
+                              "h2d_gbs": h2d / (h2d_only_ms * 1e-3) / 1e9,
+                              "note": "the step's input copies alone, 5 back to back, "
+                                      "measured right after the e2e steps"}},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,

@@ -205,27 +205,28 @@ __device__ TableSums scan_expert_table(const uint32_t* tot, uint32_t* start, uin
 }
 
 // This CTA's share of the expert table (compact CSR, expert_ids, the
-// optional scale offsets; CTA 0 also the usage stats): experts [E*b/B,
-// E*(b+1)/B) and tail entries [A + (E+1-A)*b/B, A + (E+1-A)*(b+1)/B).
+// optional scale offsets; CTA 0 also the usage stats). Thread g = b*blockDim
+// + tid of the grid takes experts g, g + B*blockDim, ... and the tail
+// entries A + g, ... (A active experts), so one CTA covers E <= blockDim.
 __device__ void write_table_share(const IdxArgs& a, const uint32_t* tot, const uint32_t* start,
                                   const uint32_t* act, const uint32_t* pad, const TableSums& t) {
-  const int E = a.E, B = gridDim.x, b = blockIdx.x;
-  const int e0 = (int)((int64_t)E * b / B), e1 = (int)((int64_t)E * (b + 1) / B);
-  for (int e = e0 + (int)threadIdx.x; e < e1; e += blockDim.x) {
+  const int E = a.E;
+  const int stride = (int)(gridDim.x * blockDim.x);
+  const int g0 = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  for (int e = g0; e < E; e += stride) {
     if (tot[e] > 0u) {
       a.expert_ids[act[e]] = e;
       a.expert_start_indices[act[e]] = start[e];
       if (a.scales_offset) a.scales_offset[act[e]] = pad[e];
     }
   }
-  const int64_t A = t.active, tail = (int64_t)E + 1 - A;
-  const int j0 = (int)(A + tail * b / B), j1 = (int)(A + tail * (b + 1) / B);
-  for (int j = j0 + (int)threadIdx.x; j < j1; j += blockDim.x) {
+  const int A = (int)t.active;
+  for (int j = A + g0; j <= E; j += stride) {
     a.expert_start_indices[j] = a.N;
     if (j < E) a.expert_ids[j] = -1;
     if (a.scales_offset) a.scales_offset[j] = t.padded_total;
   }
-  if (b == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.stats[0] = t.max_count;
     a.stats[1] = t.active;
   }
@@ -302,6 +303,12 @@ __global__ void __launch_bounds__(kRowsWarps * 32) idx_rows_kernel(const IdxArgs
 }
 
 
+// Places CTA b's 1024 slots. Before the wait each warp ranks its slots: the
+// rank of a slot is the number of earlier slots of its expert in the warp,
+// found with one match per 32 slots while the previous kernel still runs.
+// After it, base[e] = start of expert e + slots of e in earlier CTAs, the
+// warps' running offsets follow from the per-warp counts, and each slot goes
+// to base + running offset of its warp + its rank.
 template <int kBases>
 __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs a) {
   extern __shared__ uint32_t smem[];
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   __shared__ uint32_t warp_tmp[32];
   // With the count matrix from the count and rows kernels, this kernel is the
   // third of the call, so the ids (written before the count kernel ran) are
-  // complete once it starts: the warp counts overlap the rows kernel's tail.
+  // complete once it starts: the ranking overlaps the rows kernel's tail.
   // A single CTA runs right after the ids' producer and must wait first.
   if constexpr (kBases == kBasesSingleCta) wait_for_prior_grid();
 
@@ -323,19 +330,22 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
 
   const int64_t warp_base = (int64_t)blockIdx.x * kSlotsPerCta + warp * kSlotsPerWarp;
   int v[kStepsPerWarp];
+  uint32_t rank[kStepsPerWarp];
   bool bad = false;
   load_warp_slots(a, warp_base, v, bad);
-
-  // slots of each expert in this warp
+  const unsigned lower = lanemask_lt();
 #pragma unroll
   for (int s = 0; s < kStepsPerWarp; ++s) {
     const unsigned peers = __match_any_sync(kFullMask, v[s]);
+    rank[s] = v[s] >= 0 ? my_cnt[v[s]] + (uint32_t)__popc(peers & lower) : 0u;
+    __syncwarp();
     if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
     __syncwarp();
   }
   if constexpr (kBases == kBasesFromCounts) wait_for_prior_grid();  // counts, totals
   __syncthreads();
 
+  const uint32_t* s_pre = nullptr;  // slots of each expert in earlier CTAs (null: none)
   if constexpr (kBases == kBasesSingleCta) {
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
       uint32_t t = 0;
@@ -348,22 +358,20 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
   } else {
     // totals -> expert starts, active and padded offsets in one pass; every
-    // CTA writes its share of the expert table and CTA 0 the status word;
-    // then base = start + this CTA's column of prefixes over earlier CTAs
+    // CTA writes its share of the expert table and CTA 0 the status word
     __shared__ uint32_t s_flags;
     const int b = blockIdx.x;
     uint32_t* s_tot = s_pad + a.E;  // [E]
-    uint32_t* s_pre = s_tot + a.E;  // [E]
+    uint32_t* pre = s_tot + a.E;    // [E]
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
       s_tot[e] = a.totals[e];
-      s_pre[e] = a.prefix[(int64_t)e * a.row + b];
+      pre[e] = a.prefix[(int64_t)e * a.row + b];
     }
     if (threadIdx.x == 0) s_flags = 0;
     __syncthreads();
     const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
     write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
-    __syncthreads();  // the table share reads starts that other threads update next
-    for (int e = threadIdx.x; e < a.E; e += kIdxThreads) s_base[e] += s_pre[e];
+    s_pre = pre;
     if (b == 0 && !a.counts_from_router) {
       uint32_t f = 0;
       for (int j = threadIdx.x; j < a.num_blocks; j += kIdxThreads) f |= a.flags[j];
@@ -373,10 +381,10 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
       if (threadIdx.x == 0) *a.status = s_flags;
     }
   }
-  __syncthreads();
-  // per-warp running offsets: base + slots of e in earlier warps
+  // per-warp running offsets: base + slots of e in earlier warps (the expert
+  // table above only reads the starts, so no barrier is needed before this)
   for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
-    uint32_t run = s_base[e];
+    uint32_t run = s_base[e] + (s_pre ? s_pre[e] : 0u);
     for (int w = 0; w < kIdxWarps; ++w) {
       const uint32_t c = s_warp[w * a.E + e];
       s_warp[w * a.E + e] = run;
@@ -385,23 +393,17 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   }
   __syncthreads();
 
-  const unsigned lower = lanemask_lt();
 #pragma unroll
   for (int s = 0; s < kStepsPerWarp; ++s) {
     const int64_t i = warp_base + s * 32 + lane;
-    const unsigned peers = __match_any_sync(kFullMask, v[s]);
-    uint32_t pos = 0xFFFFFFFFu;
-    if (v[s] >= 0) pos = my_cnt[v[s]] + (uint32_t)__popc(peers & lower);
-    __syncwarp();
-    if (v[s] >= 0 && lane == __ffs(peers) - 1) my_cnt[v[s]] += (uint32_t)__popc(peers);
-    __syncwarp();
     if (i < (int64_t)a.N) {
+      const uint32_t pos = v[s] >= 0 ? my_cnt[v[s]] + rank[s] : 0xFFFFFFFFu;
       a.restore_token_order[i] = pos;
       if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
     }
   }
   if constexpr (kBases == kBasesFromCounts) {
-    if (a.counts_from_router && __syncthreads_or(bad) && threadIdx.x == 0)
+    if (a.counts_from_router && __any_sync(kFullMask, bad) && lane == 0)
       atomicOr(a.status, MOE_DEVICE_STATUS_BAD_EXPERT_ID);
   }
 }
