@@ -415,6 +415,50 @@ def time_graph_replay(fn, n: int, dev, reps: int = 10):
     return e0.elapsed_time(e1) * 1e3 / (reps * n)
 
 
+def host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h):
+    """The host link right after the e2e steps, in the same process: the step's
+    input copies alone (5 back to back), the same copies with the output copy
+    of each step behind them but no compute (10 steps, pipelined as in the
+    e2e steps), and 20 more e2e steps. Its throughput moves by 10-20% between
+    boxes and runs, so the e2e value is read against these."""
+    import torch
+
+    def window(submit, first, last, n):
+        for i in range(2):
+            submit(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(first)
+        for i in range(n):
+            submit(i + 2)
+        e1.record(last)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def inputs(i):
+        slot = streamer.slots[i % 2]
+        with torch.cuda.stream(streamer.copy_in):
+            slot["scores"].copy_(s_h, non_blocking=True)
+            slot["bias"].copy_(b_h, non_blocking=True)
+            slot["down"].copy_(down_h, non_blocking=True)
+            slot["copied_in"].record(streamer.copy_in)
+
+    def copies(i):
+        inputs(i)
+        slot = streamer.slots[i % 2]
+        streamer.copy_out.wait_event(slot["copied_in"])
+        with torch.cuda.stream(streamer.copy_out):
+            outs_h[i % 2].copy_(slot["out"], non_blocking=True)
+
+    return {
+        "h2d_only_ms": window(inputs, streamer.copy_in, streamer.copy_in, 5),
+        "copies_only_ms": window(copies, streamer.copy_in, streamer.copy_out, 10),
+        "e2e_again_ms": window(lambda i: streamer.submit(s_h, b_h, down_h, outs_h[i % 2]),
+                               streamer.copy_in, streamer.copy_out, 20),
+        "note": "ms per step: input copies alone; input and output copies pipelined without "
+                "compute; 20 more e2e steps"}
+
+
 def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     """The router alone, launched back to back: on the workload's batch
     rotating over copies whose total exceeds L2 twice over, on a 262144-token
@@ -747,21 +791,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     streamer.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
     h2d, d2h = pipe.host_bytes()
-    # The host link in the same run: the step's input copies alone, back to
-    # back on the copy-in stream (its throughput moves by about 10% between
-    # runs on this kind of host, so e2e is read against this figure).
-    slot = streamer.slots[0]
-    with torch.cuda.stream(streamer.copy_in):
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(streamer.copy_in)
-        for _ in range(5):
-            slot["scores"].copy_(s_h, non_blocking=True)
-            slot["bias"].copy_(b_h, non_blocking=True)
-            slot["down"].copy_(down_h, non_blocking=True)
-        c1.record(streamer.copy_in)
-    streamer.synchronize()
-    h2d_only_ms = c0.elapsed_time(c1) / 5
+    host_link = host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h)
 
     if rank != 0:
         if world > 1:
@@ -844,10 +874,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
                 "timing": "steady state: the timed steps follow three untimed ones in stream "
                           "order; events on the copy-in stream at the start and the copy-out "
                           "stream at the end",
-                "host_link": {"h2d_ms_per_step": h2d_only_ms,
-                              "h2d_gbs": h2d / (h2d_only_ms * 1e-3) / 1e9,
-                              "note": "the step's input copies alone, 5 back to back, "
-                                      "measured right after the e2e steps"}},
+                "host_link": dict(host_link, h2d_gbs=h2d / (host_link["h2d_only_ms"] * 1e-3)
+                                  / 1e9)},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,

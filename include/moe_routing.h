@@ -62,7 +62,7 @@ typedef enum {
  * and (when given a status pointer) moe_finalize_ex and moe_permute. */
 #define MOE_DEVICE_STATUS_BAD_EXPERT_ID 0x1u /* some topk_ids entry was outside [0, E) */
 #define MOE_DEVICE_STATUS_SYNC_TIMEOUT 0x2u  /* single-launch route+index: a cross-CTA wait gave up */
-#define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* single-launch route+index: inconsistent counts */
+#define MOE_DEVICE_STATUS_SYNC_STATE 0x4u    /* route+index: inconsistent counts (workspace not zero-filled) */
 #define MOE_DEVICE_STATUS_BAD_RESTORE_ORDER 0x8u /* finalize/permute: an entry >= T*K */
 
 /* Limits of this implementation. */
@@ -224,6 +224,10 @@ size_t moe_route_index_workspace_size(int64_t num_tokens, int32_t n_routed_exper
  *   bytes, 256-byte aligned, caller-owned, ZERO-FILLED before its first use
  *   (e.g. cudaMemset): the router's counts accumulate into it, and every call
  *   leaves them zero again, so the workspace is zeroed once, not per call.
+ *   Counts that do not add up to T*K (a workspace that was not zero-filled)
+ *   set MOE_DEVICE_STATUS_SYNC_STATE; the index outputs are then unspecified,
+ *   no position at or past T*K is written, and the call leaves the counts it
+ *   used zero, so the next call on the same shapes is correct again.
  *   The prefix matrix is placed at the end of workspace_bytes, so one
  *   workspace may serve calls of any shapes that fit it, in any order.
  *   Word 0 receives the device status word (moe_read_device_status). Calls

@@ -16,10 +16,11 @@
 //   rows    : one warp per expert turns its row into exclusive prefixes,
 //             counts[e][b] := sum_{b' < b} counts[e][b'], and writes the total
 //             tot[e]; each warp instruction covers 128 consecutive counts.
+//             CTA 0 zeroes the device status word.
 //   scatter : CTA b scans the totals into expert starts start(e) and writes
 //             its share of the compact CSR, expert_ids and scale offsets (CTA
-//             0 also the usage stats and the device status word), reads its
-//             column of prefixes, and re-reads its
+//             0 also the usage stats, and ORs the count flags into the status
+//             word), reads its column of prefixes, and re-reads its
 //             slots; within a CTA each warp owns 128 consecutive slots, so a
 //             slot's position is start(e) + counts[e][b] + (slots of e in
 //             earlier warps) + (slots of e in earlier steps of its warp) +

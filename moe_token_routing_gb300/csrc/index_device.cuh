@@ -128,7 +128,7 @@ __device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act
 
 // Sums that the expert table needs besides the per-expert arrays.
 struct TableSums {
-  uint32_t active, padded_total, max_count;
+  uint32_t slots, active, padded_total, max_count;
 };
 
 // From tot[0..E) (shared memory), every thread of the block computes, in one
@@ -198,6 +198,7 @@ __device__ TableSums scan_expert_table(const uint32_t* tot, uint32_t* start, uin
   const uint4 t = s_total;
   __syncthreads();
   TableSums r;
+  r.slots = t.x;
   r.active = t.y;
   r.padded_total = t.z;
   r.max_count = t.w;
@@ -267,9 +268,9 @@ enum BaseSource : int {
 // row is left zero for the next call's atomics, in the same coalesced pass.
 __global__ void __launch_bounds__(kRowsWarps * 32) idx_rows_kernel(const IdxArgs a) {
   wait_for_prior_grid();
-  // counts from the router: no count kernel wrote flags, so the status word
-  // starts here and the scatter CTAs add their bits to it
-  if (a.counts_from_router && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+  // the status word starts here; the scatter CTAs add their bits to it (and
+  // the count kernel's flags, when there is one)
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRowsWarps + (threadIdx.x >> 5);
   if (e >= a.E) return;
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   __syncthreads();
 
   const uint32_t* s_pre = nullptr;  // slots of each expert in earlier CTAs (null: none)
+  bool consistent = true;
   if constexpr (kBases == kBasesSingleCta) {
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
       uint32_t t = 0;
@@ -358,7 +360,8 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
   } else {
     // totals -> expert starts, active and padded offsets in one pass; every
-    // CTA writes its share of the expert table and CTA 0 the status word
+    // CTA writes its share of the expert table, and CTA 0 ORs the count
+    // kernel's flags (if any) into the status word the rows kernel zeroed
     __shared__ uint32_t s_flags;
     const int b = blockIdx.x;
     uint32_t* s_tot = s_pad + a.E;  // [E]
@@ -372,13 +375,18 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
     const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
     write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
     s_pre = pre;
+    // counts that do not add up to N can only come from a workspace that was
+    // not zero-filled: reported, and no slot is placed (every position below
+    // is also checked against N, so no write leaves the outputs)
+    consistent = sums.slots == a.N;
+    if (!consistent && b == 0 && threadIdx.x == 0) atomicOr(a.status, MOE_DEVICE_STATUS_SYNC_STATE);
     if (b == 0 && !a.counts_from_router) {
       uint32_t f = 0;
       for (int j = threadIdx.x; j < a.num_blocks; j += kIdxThreads) f |= a.flags[j];
       f = __reduce_or_sync(kFullMask, f);
       if (lane == 0 && f) atomicOr(&s_flags, f);
       __syncthreads();
-      if (threadIdx.x == 0) *a.status = s_flags;
+      if (threadIdx.x == 0 && s_flags) atomicOr(a.status, s_flags);
     }
   }
   // per-warp running offsets: base + slots of e in earlier warps (the expert
@@ -393,18 +401,28 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   }
   __syncthreads();
 
+  bool overflow = false;
+  if (consistent) {
 #pragma unroll
-  for (int s = 0; s < kStepsPerWarp; ++s) {
-    const int64_t i = warp_base + s * 32 + lane;
-    if (i < (int64_t)a.N) {
-      const uint32_t pos = v[s] >= 0 ? my_cnt[v[s]] + rank[s] : 0xFFFFFFFFu;
-      a.restore_token_order[i] = pos;
-      if (v[s] >= 0) a.token_expert_order[pos] = (uint32_t)i;
+    for (int s = 0; s < kStepsPerWarp; ++s) {
+      const int64_t i = warp_base + s * 32 + lane;
+      if (i < (int64_t)a.N) {
+        const uint32_t pos = v[s] >= 0 ? my_cnt[v[s]] + rank[s] : 0xFFFFFFFFu;
+        a.restore_token_order[i] = pos;
+        if (v[s] >= 0) {
+          if (pos < a.N)
+            a.token_expert_order[pos] = (uint32_t)i;
+          else
+            overflow = true;
+        }
+      }
     }
   }
   if constexpr (kBases == kBasesFromCounts) {
-    if (a.counts_from_router && __any_sync(kFullMask, bad) && lane == 0)
-      atomicOr(a.status, MOE_DEVICE_STATUS_BAD_EXPERT_ID);
+    uint32_t bits = 0;
+    if (a.counts_from_router && __any_sync(kFullMask, bad)) bits |= MOE_DEVICE_STATUS_BAD_EXPERT_ID;
+    if (__any_sync(kFullMask, overflow)) bits |= MOE_DEVICE_STATUS_SYNC_STATE;
+    if (bits && lane == 0) atomicOr(a.status, bits);
   }
 }
 

@@ -196,6 +196,31 @@ def test_call_counter_advances_and_calls_repeat():
         assert header.tolist() == [0, n]
 
 
+@pytest.mark.parametrize("name", ["dsv3_prefill", "skewed_ungrouped"])
+def test_unzeroed_workspace_is_reported(name):
+    """A workspace that was not zero-filled (every word 1, so each count of
+    this shape is one too high and the totals exceed T*K) sets
+    MOE_DEVICE_STATUS_SYNC_STATE; the guard regions around every output and
+    the workspace stay intact (no position at or past T*K is written), and
+    the call leaves the counts it used zero, so the next call is exact."""
+    moe = _moe()
+    cfg, scores, bias, ids_ref, w_ref, idx_ref = workload(name)
+    bufs = moe.RouteIndexBuffers(cfg.T, cfg.E, cfg.K, "cuda")
+    ws, gws = guarded((bufs.workspace.numel(),), torch.uint8, fill=0, name="workspace")
+    ws.view(torch.int32).fill_(1)
+    bufs.workspace = ws
+    bufs._guards = guard_attrs(bufs, ("expert_indices", "expert_weights") + INDEX_KEYS) + [gws]
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                                bufs=bufs)
+    # the routing itself does not read the workspace
+    assert np.array_equal(got["ids"], ids_ref)
+    assert bufs.device_status() & moe.DEVICE_STATUS_SYNC_STATE
+    got, bufs = gpu_route_index(scores, bias, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale,
+                                bufs=bufs)
+    assert_parity(got, ids_ref, w_ref, idx_ref, cfg.E)
+    assert bufs.device_status() == 0
+
+
 @BOTH
 def test_workspace_reused_across_shapes(single):
     """One workspace, sized for the largest call, serves calls of other shapes
