@@ -54,8 +54,8 @@ def parse_args():
                         "instead of the fused moe_route_index")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the router back-to-back / large-batch measurements and the "
-                        "secondary workloads (profiling runs)")
+                   help="skip the router back-to-back / large-batch measurements, the "
+                        "secondary workloads and the host-link windows (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args()
@@ -499,6 +499,14 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     hb = {}
     b2b = time_back_to_back(f, n, stream, hb)
     graph_b2b = time_graph_replay(f, n, dev)
+    # the same bytes read by a library reduction (torch.sum over each score
+    # copy, into a preallocated scalar), replayed the same way: what one launch
+    # that only reads the scores costs on this GPU
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def read_fn(i, st=None):
+        torch.sum(bufs[i % len(bufs)], dim=(0, 1), out=acc)
+    read_graph = time_graph_replay(read_fn, n, dev)
     del bufs
     big_T = 262144
     big = torch.from_numpy(synth.make_scores(cfg.replace(T=big_T))).to(dev)
@@ -543,7 +551,8 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
                     "per launch",
             "back_to_back": graph_entry(graph_b2b, rb),
             "large_batch": graph_entry(big_graph, bb),
-            "launch_floor_us": floor_graph},
+            "launch_floor_us": floor_graph,
+            "read_only_kernel": graph_entry(read_graph, 4 * T * E)},
         "hbm_time_at_peak_us": rb / (peak * 1e3),
         "residue_over_hbm_time_us": b2b - rb / (peak * 1e3),
     }
@@ -791,7 +800,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
     streamer.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
     h2d, d2h = pipe.host_bytes()
-    host_link = host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h)
+    host_link = (None if args.no_extras
+                 else host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h))
 
     if rank != 0:
         if world > 1:
@@ -874,8 +884,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
                 "timing": "steady state: the timed steps follow three untimed ones in stream "
                           "order; events on the copy-in stream at the start and the copy-out "
                           "stream at the end",
-                "host_link": dict(host_link, h2d_gbs=h2d / (host_link["h2d_only_ms"] * 1e-3)
-                                  / 1e9)},
+                "host_link": host_link and dict(
+                    host_link, h2d_gbs=h2d / (host_link["h2d_only_ms"] * 1e-3) / 1e9)},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,
