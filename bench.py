@@ -558,9 +558,12 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     }
 
 
-def secondary_workload(moe, name, dev, stream, peak, flush_l2, reps=50):
-    """Route + index and finalize stage times of another large workload
-    (separate passes, L2 flushed before each call)."""
+def secondary_workload(moe, name, dev, stream, peak, flush_l2, reps=50, graph_steps=0):
+    """Route + index and finalize stage times of another workload (separate
+    passes, L2 flushed before each call); with graph_steps > 0 also the time
+    per whole step when that many steps, captured in a CUDA graph, replay
+    back to back (no host work between launches; the inputs stay wherever
+    the previous step left them)."""
     import statistics
 
     import torch
@@ -594,6 +597,9 @@ def secondary_workload(moe, name, dev, stream, peak, flush_l2, reps=50):
            "tokens_per_s": c.T / ((ri + fin) * 1e-3),
            "finalize_gbs": fb / (fin * 1e-3) / 1e9, "finalize_frac": fb / (fin * 1e-3) / 1e9 / peak,
            "finalize_algorithmic_bytes": fb, "device_status_clean": ok, "reps": reps}
+    if graph_steps > 0:
+        out["graph_replay_step_us"] = time_graph_replay(
+            lambda i, st: pipe(scores, bias, down, stream=st), graph_steps, dev)
     del pipe, scores, bias, down
     torch.cuda.empty_cache()
     return out
@@ -770,9 +776,11 @@ def run_gpu(args, cfg, rank, world, local_rank):
     extras = {}
     if rank == 0 and not args.no_extras:
         extras["router"] = router_evidence(moe, cfg, s_d, b_d, dev, stream, peak_gbs)
-        for name in ("skewed_ungrouped", "few_expert_large_batch"):
+        for name in ("skewed_ungrouped", "few_expert_large_batch", "dsv3_decode"):
             if name != cfg.name:
-                extras[name] = secondary_workload(moe, name, dev, stream, peak_gbs, flush_l2)
+                extras[name] = secondary_workload(
+                    moe, name, dev, stream, peak_gbs, flush_l2,
+                    graph_steps=32 if name == "dsv3_decode" else 0)
 
     # ---- end to end through the host-buffer API: pinned inputs copied in and the
     # output copied back every step, copies of consecutive steps overlapped

@@ -84,3 +84,55 @@ def test_host_streamer_overlapped_batches():
     for got, exp in zip(outs, expected):
         assert torch.equal(got.view(torch.int16), exp.view(torch.int16))
     assert not torch.equal(expected[0].view(torch.int16), expected[1].view(torch.int16))
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["route_index", "separate"])
+@pytest.mark.parametrize("name", ["dsv3_decode", "skewed_ungrouped"])
+def test_cuda_graph_replay(name, fused):
+    """One step captured in a CUDA graph: replaying it three times on the same
+    inputs gives the oracle's outputs every time (the index workspace carries
+    nothing from one replay into the next), and after new inputs are copied
+    into the captured buffers a replay gives the oracle's outputs for those."""
+    cfg, scores, bias, ids, w, idx = workload(name)
+    down = workload_down(name)
+    pipe = _pipe(cfg, fused)
+    s_d = torch.from_numpy(scores).cuda()
+    b_d = torch.from_numpy(bias).cuda()
+    d_d = torch.from_numpy(down.view(np.int16)).cuda().view(torch.bfloat16)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        pipe(s_d, b_d, d_d, stream=st)  # first calls outside the capture (module load)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        pipe(s_d, b_d, d_d, stream=st)
+
+    def check(ids_ref, w_ref, idx_ref, fin_ref):
+        torch.cuda.synchronize()
+        assert np.array_equal(pipe.expert_indices.cpu().numpy(), ids_ref)
+        assert np.array_equal(pipe.expert_weights.cpu().numpy().view(np.uint32),
+                              w_ref.view(np.uint32))
+        for k in ("token_expert_order", "restore_token_order", "expert_start_indices"):
+            assert np.array_equal(getattr(pipe.index, k).cpu().numpy().view(np.uint32),
+                                  idx_ref[k]), k
+        got = pipe.output.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, f32_to_bf16_bits(fin_ref))
+        assert pipe.device_status() == 0
+
+    for _ in range(3):
+        pipe.output.zero_()
+        pipe.index.token_expert_order.fill_(-1)
+        graph.replay()
+        check(ids, w, idx, workload_finalize_ref(name))
+    # another seed's inputs, copied into the captured buffers
+    import oracle
+    c2 = cfg.replace(seed=cfg.seed + 1)
+    scores2, bias2, down2 = synth.make_scores(c2), synth.make_bias(c2), synth.make_down(c2)
+    ids2, w2 = oracle.route(scores2, bias2, cfg.K, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    idx2 = oracle.create_indices(ids2, cfg.E)
+    fin2 = oracle.finalize(down2, idx2["restore_token_order"], w2, cfg.T, cfg.K, cfg.H)
+    s_d.copy_(torch.from_numpy(scores2))
+    b_d.copy_(torch.from_numpy(bias2))
+    d_d.view(torch.int16).copy_(torch.from_numpy(down2.view(np.int16)))
+    graph.replay()
+    check(ids2, w2, idx2, fin2)
