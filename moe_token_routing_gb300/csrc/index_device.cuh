@@ -1,7 +1,7 @@
 // Device code of the expert index builder (page "moe_create_indices"),
 // shared by the index kernels and the fused router + index kernel: the
-// argument block, block-wide scans and the expert table (compact CSR,
-// expert_ids, usage stats, aligned scale offsets).
+// argument block, the blocked scan of the expert totals and the expert table
+// (compact CSR, expert_ids, usage stats, aligned scale offsets).
 #pragma once
 
 #include "common.cuh"
@@ -36,95 +36,6 @@ struct IdxArgs {
   int num_blocks;
   int row;
 };
-
-// ---------------------------------------------------------------- block helpers
-// Exclusive prefix sum of data[0..n) in shared memory, in place; all threads of
-// the block call it. Returns the total.
-__device__ uint32_t block_exclusive_scan(uint32_t* data, int n, uint32_t* warp_tmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
-  const int beg = min((int)threadIdx.x * per, n), end = min(beg + per, n);
-  uint32_t local = 0;
-  for (int i = beg; i < end; ++i) local += data[i];
-  uint32_t x = local;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFullMask, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) warp_tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t v = lane < nwarps ? warp_tmp[lane] : 0u;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFullMask, v, off);
-      if (lane >= off) v += y;
-    }
-    warp_tmp[lane] = v;
-  }
-  __syncthreads();
-  uint32_t run = x - local + (warp > 0 ? warp_tmp[warp - 1] : 0u);
-  const uint32_t total = warp_tmp[nwarps - 1];
-  for (int i = beg; i < end; ++i) {
-    const uint32_t v = data[i];
-    data[i] = run;
-    run += v;
-  }
-  __syncthreads();
-  return total;
-}
-
-__device__ uint32_t block_max(uint32_t v, uint32_t* warp_tmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  v = __reduce_max_sync(kFullMask, v);
-  if (lane == 0) warp_tmp[warp] = v;
-  __syncthreads();
-  uint32_t r = 0;
-  for (int w = 0; w < nwarps; ++w) r = max(r, warp_tmp[w]);
-  __syncthreads();
-  return r;
-}
-
-// Given per-expert totals tot[0..E) in shared memory: writes the compact CSR,
-// expert_ids and usage stats (and, if requested, the 128-row aligned scale
-// offsets), and turns tot[] into each expert's start offset. `act` and `pad`
-// are E words of shared scratch each.
-__device__ void emit_expert_table(const IdxArgs& a, uint32_t* tot, uint32_t* act, uint32_t* pad,
-                                  uint32_t* warp_tmp, bool write = true) {
-  const bool want_scales = a.scales_offset != nullptr;
-  uint32_t local_max = 0;
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-    act[e] = tot[e] > 0u;
-    if (want_scales) pad[e] = (tot[e] + (kScaleRowAlign - 1)) / kScaleRowAlign * kScaleRowAlign;
-    local_max = max(local_max, tot[e]);
-  }
-  __syncthreads();
-  const uint32_t max_count = block_max(local_max, warp_tmp);
-  const uint32_t active = block_exclusive_scan(act, a.E, warp_tmp);
-  block_exclusive_scan(tot, a.E, warp_tmp);  // tot[e] := start of expert e
-  const uint32_t padded_total = want_scales ? block_exclusive_scan(pad, a.E, warp_tmp) : 0u;
-  if (!write) return;
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-    const bool is_active = (e + 1 < a.E ? act[e + 1] : active) != act[e];
-    if (is_active) {
-      a.expert_ids[act[e]] = e;
-      a.expert_start_indices[act[e]] = tot[e];
-      if (want_scales) a.scales_offset[act[e]] = pad[e];
-    }
-  }
-  for (int j = (int)active + threadIdx.x; j <= a.E; j += blockDim.x) {
-    a.expert_start_indices[j] = a.N;
-    if (j < a.E) a.expert_ids[j] = -1;
-    if (want_scales) a.scales_offset[j] = padded_total;
-  }
-  if (threadIdx.x == 0) {
-    a.stats[0] = max_count;
-    a.stats[1] = active;
-  }
-}
 
 // Sums that the expert table needs besides the per-expert arrays.
 struct TableSums {
@@ -317,7 +228,6 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   uint32_t* s_base = s_warp + kIdxWarps * a.E;  // [E]
   uint32_t* s_act = s_base + a.E;               // [E]
   uint32_t* s_pad = s_act + a.E;                // [E]; then [E] totals, [E] prefixes
-  __shared__ uint32_t warp_tmp[32];
   // With the count matrix from the count and rows kernels, this kernel is the
   // third of the call, so the ids (written before the count kernel ran) are
   // complete once it starts: the ranking overlaps the rows kernel's tail.
@@ -349,13 +259,18 @@ __global__ void __launch_bounds__(kIdxThreads) idx_scatter_kernel(const IdxArgs 
   const uint32_t* s_pre = nullptr;  // slots of each expert in earlier CTAs (null: none)
   bool consistent = true;
   if constexpr (kBases == kBasesSingleCta) {
+    // the totals are the sums of the warps' counts; one blocked pass turns
+    // them into the starts, active and padded offsets, and this CTA writes
+    // the whole expert table
+    uint32_t* s_tot = s_pad + a.E;  // [E]
     for (int e = threadIdx.x; e < a.E; e += kIdxThreads) {
       uint32_t t = 0;
       for (int w = 0; w < kIdxWarps; ++w) t += s_warp[w * a.E + e];
-      s_base[e] = t;
+      s_tot[e] = t;
     }
     __syncthreads();
-    emit_expert_table(a, s_base, s_act, s_pad, warp_tmp);
+    const TableSums sums = scan_expert_table(s_tot, s_base, s_act, s_pad, a.E);
+    write_table_share(a, s_tot, s_base, s_act, s_pad, sums);
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) *a.status = any_bad ? MOE_DEVICE_STATUS_BAD_EXPERT_ID : 0u;
   } else {
