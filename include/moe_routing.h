@@ -256,7 +256,7 @@ size_t moe_route_index_single_launch_workspace_size(int64_t num_tokens,
 /*
  * moe_route_index_single_launch -- the same outputs as moe_route_index from
  * ONE cooperative kernel launch. On the measured shapes it is the slower of
- * the two (DeepSeek-V3-shaped prefill, 16384 tokens: 32.7 us against 21.0 us
+ * the two (DeepSeek-V3-shaped prefill, 16384 tokens: 31.6 us against 19.5 us
  * for moe_route_index on one GB300); it suits callers that want a single
  * launch per batch.
  * Every output is bit-identical to those of the two separate calls:
