@@ -26,9 +26,10 @@
 //            totals into expert starts, and each warp places its slots, 32
 //            per step: start(e) + pre[e][b] + slots of e in earlier warps of
 //            the CTA + earlier steps + lower lanes of the step with the same e
-//            (match.any). CTA 0 then writes the CSR, expert_ids, stats and
-//            scale offsets, gathers every CTA's status bits into the status
-//            word and advances the call counter.
+//            (match.any). Every CTA writes its share of the CSR, expert_ids
+//            and scale offsets (CTA 0 also the stats); CTA 0 then gathers
+//            every CTA's status bits into the status word and advances the
+//            call counter.
 // Every published value is a 64-bit word tagged with this call's number (see
 // tagged_sync.cuh), so a consumer checks the data itself and no fence sits on
 // the critical path. Two relaxed counters (CTAs that published their counts,
