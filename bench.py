@@ -415,6 +415,34 @@ def time_graph_replay(fn, n: int, dev, reps: int = 10):
     return e0.elapsed_time(e1) * 1e3 / (reps * n)
 
 
+def router_roofline(single_gbs, single_ms, peak, nbytes, evidence):
+    """The router's roofline entry. Its headline is the per-launch time of 48
+    launches back to back between one event pair (inputs rotating over more
+    than twice the L2), the steady state of a stream of batches; one launch
+    between two events after an L2 flush carries the event-to-kernel latency
+    too and is reported beside it. Without the back-to-back evidence (a
+    --no-extras run) the single launch is the headline."""
+    single = {"us_per_launch": single_ms * 1e3, "achieved_gbs": single_gbs,
+              "frac": single_gbs / peak,
+              "timing": "one launch between two events after an L2 flush, mean of the stage pass"}
+    out = {"bound": "hbm", "peak": peak, "unit": "GB/s", "algorithmic_bytes_per_launch": nbytes}
+    if evidence and evidence.get("back_to_back"):
+        b2b = evidence["back_to_back"]
+        gbs = b2b["achieved_gbs"]
+        out.update({"achieved": gbs, "frac": gbs / peak,
+                    "frac_vs_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                    "timing": "48 launches back to back from the host between one event pair, "
+                              "inputs rotating over more than twice the L2"})
+    else:
+        out.update({"achieved": single_gbs, "frac": single_gbs / peak,
+                    "frac_vs_nominal_8tbs": single_gbs / NOMINAL_HBM_GBS,
+                    "timing": single["timing"]})
+    out["single_launch"] = single
+    if evidence:
+        out.update(evidence)
+    return out
+
+
 def host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h):
     """The host link right after the e2e steps, in the same process: the step's
     input copies alone (5 back to back), the same copies with the output copy
@@ -846,12 +874,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": nbytes["finalize"],
                      "traffic": profile_traffic("finalize.cu", "finalize_dsv3_prefill.txt")
                      if cfg.name == "dsv3_prefill" else None},
-        "router_roofline": dict({"bound": "hbm", "achieved": route_gbs, "peak": peak,
-                                 "unit": "GB/s", "frac": route_gbs / peak,
-                                 "frac_vs_nominal_8tbs": route_gbs / NOMINAL_HBM_GBS,
-                                 "algorithmic_bytes_per_launch": nbytes["route"],
-                                 "timing": "single launch, L2 flushed, mean of the stage pass"},
-                                **extras.get("router", {})),
+        "router_roofline": router_roofline(route_gbs, route_mean, peak, nbytes["route"],
+                                           extras.get("router")),
         "secondary_workloads": {k: v for k, v in extras.items() if k != "router"},
         "stages_ms": {"route": route_mean, "create_indices": statistics.fmean(index_ms),
                       "route_index_fused": statistics.fmean(fused_ms),

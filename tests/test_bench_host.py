@@ -56,3 +56,18 @@ def test_default_arguments(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--separate-index", "--steps", "7"])
     a = bench.parse_args()
     assert a.separate_index and a.steps == 7
+
+
+def test_router_roofline_headline():
+    """The router's headline is the back-to-back launches when they were
+    measured, and the single launch (kept beside it) otherwise."""
+    import bench
+    ev = {"back_to_back": {"us_per_launch": 8.0, "achieved_gbs": 2000.0, "frac": 0.3}}
+    r = bench.router_roofline(1500.0, 0.012, 6787.6, 17826816, ev)
+    assert r["achieved"] == 2000.0 and abs(r["frac"] - 2000.0 / 6787.6) < 1e-12
+    assert r["single_launch"]["achieved_gbs"] == 1500.0
+    assert abs(r["single_launch"]["us_per_launch"] - 12.0) < 1e-9
+    assert r["back_to_back"] is ev["back_to_back"]
+    r = bench.router_roofline(1500.0, 0.012, 6787.6, 17826816, None)
+    assert r["achieved"] == 1500.0
+    assert r["timing"] == r["single_launch"]["timing"]
