@@ -74,6 +74,21 @@ MUTANTS = {
                                   "const float n = std::trunc(x * 1.44269504088896341f);"),
     "permute copies the slot's row": ("out[p * H + h] = input[t * H + h];",
                                       "out[p * H + h] = input[(p / K) * H + h];"),
+    "one group too many kept": (
+        "for (int32_t m = 0; m < topk_group; ++m) {",
+        "for (int32_t m = 0; m < topk_group + (topk_group < n_groups ? 1 : 0); ++m) {"),
+    "group score from the unbiased scores": (
+        "group_vals.assign(b.begin() + j * S, b.begin() + (j + 1) * S);",
+        "group_vals.assign(s + j * S, s + (j + 1) * S);"),
+    "normalisation sum skips the first weight": (
+        "for (int32_t k = 0; k < K; ++k) sum = sum + w[k];",
+        "for (int32_t k = 1; k < K; ++k) sum = sum + w[k];"),
+    "CSR starts one past": ("expert_start_indices[active] = offset;",
+                            "expert_start_indices[active] = offset + 1;"),
+    "expert_ids tail padded with 0": ("for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
+                                      "expert_ids[j] = -1;",
+                                      "for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
+                                      "expert_ids[j] = 0;"),
 }
 
 
