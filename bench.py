@@ -527,13 +527,13 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     hb = {}
     b2b = time_back_to_back(f, n, stream, hb)
     graph_b2b = time_graph_replay(f, n, dev)
-    # the same bytes read by a library reduction (torch.sum over each score
-    # copy, into a preallocated scalar), replayed the same way: what one launch
-    # that only reads the scores costs on this GPU
-    acc = torch.empty((), dtype=torch.float32, device=dev)
+    # the same bytes read by a library reduction (torch.sum of each score row,
+    # into a preallocated vector), replayed the same way: what one launch that
+    # only reads the scores costs with a stock kernel on this GPU
+    acc = torch.empty((T,), dtype=torch.float32, device=dev)
 
     def read_fn(i, st=None):
-        torch.sum(bufs[i % len(bufs)], dim=(0, 1), out=acc)
+        torch.sum(bufs[i % len(bufs)], dim=1, out=acc)
     read_graph = time_graph_replay(read_fn, n, dev)
     del bufs
     big_T = 262144
