@@ -80,4 +80,23 @@ moe_status_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem
   return launch_status();
 }
 
+// Launches `kernel` fully ordered after the preceding work on `stream` (no
+// programmatic serialisation; its wait_for_prior_grid returns at once).
+template <typename... KArgs, typename... Args>
+moe_status_t launch_ordered(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 }  // namespace moe

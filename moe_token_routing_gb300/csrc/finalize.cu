@@ -167,10 +167,16 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
 // resident CTAs striding over the tokens ends unevenly (at 4 CTAs per SM and
 // 16384 tokens some CTAs take 27 tokens, others 26) and measured about 1.3%
 // slower. The token loop still strides, for T beyond the grid limit.
+// A decode-sized batch (fewer tokens than four CTAs per SM) launches fully
+// ordered after the index build: with programmatic serialisation a decode
+// step (route + index + finalize, 128 tokens, replayed from a CUDA graph)
+// measured 10.9 us against 10.3 us without it.
 template <typename Kernel>
 moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream) {
   const int64_t cap = 0x7fffffff;
   const int grid = (int)(a.T < cap ? a.T : cap);
+  if (a.T < 4 * (int64_t)device_info().sm_count)
+    return launch_ordered(k, grid, kFinThreads, 0, stream, a);
   return launch(k, grid, kFinThreads, 0, stream, a);
 }
 
