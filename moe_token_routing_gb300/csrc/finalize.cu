@@ -86,8 +86,10 @@ __device__ __forceinline__ void store_chunk(void* out, int64_t t, int64_t H8, in
 }
 
 // K known at compile time: all K row loads of kChunkUnroll chunks in flight.
-template <int K, typename WT, typename OT>
-__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) {
+// kThreads per CTA (one CTA per token): kFinThreads, or more for small
+// batches so that a token's row takes fewer dependent rounds of loads.
+template <int K, typename WT, typename OT, int kThreads = kFinThreads>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
     int64_t row[K];
@@ -103,18 +105,18 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinArgs a) 
       w[k] = load_weight<WT>(a.weight, t * K + k);
     }
     if (!all_ok && threadIdx.x == 0) report_bad_restore(a.status);
-    for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kFinThreads * kChunkUnroll) {
+    for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kThreads * kChunkUnroll) {
       uint4 v[kChunkUnroll][K];
 #pragma unroll
       for (int u = 0; u < kChunkUnroll; ++u) {
-        const int64_t c = c0 + (int64_t)u * kFinThreads;
+        const int64_t c = c0 + (int64_t)u * kThreads;
 #pragma unroll
         for (int k = 0; k < K; ++k)
           v[u][k] = (c < a.H8 && ok[k]) ? load_stream(a.down + row[k] + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kChunkUnroll; ++u) {
-        const int64_t c = c0 + (int64_t)u * kFinThreads;
+        const int64_t c = c0 + (int64_t)u * kThreads;
         if (c >= a.H8) break;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -172,12 +174,31 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
 // step (route + index + finalize, 128 tokens, replayed from a CUDA graph)
 // measured 10.9 us against 10.3 us without it.
 template <typename Kernel>
-moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream) {
+moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream,
+                        int threads = kFinThreads) {
   const int64_t cap = 0x7fffffff;
   const int grid = (int)(a.T < cap ? a.T : cap);
   if (a.T < 4 * (int64_t)device_info().sm_count)
-    return launch_ordered(k, grid, kFinThreads, 0, stream, a);
-  return launch(k, grid, kFinThreads, 0, stream, a);
+    return launch_ordered(k, grid, threads, 0, stream, a);
+  return launch(k, grid, threads, 0, stream, a);
+}
+
+// K fixed at compile time. When a row needs more than one round of loads at
+// kFinThreads threads, a batch with at most one token per SM takes up to 512
+// threads per token and one with at most two up to 256 (still one wave of
+// CTAs at the registers a thread holds): a decode token's row of H = 7168
+// then takes one round instead of four, and a decode step (route + index +
+// finalize, 128 tokens, replayed from a CUDA graph) measured 9.4 us against
+// 10.2 us. Short rows keep kFinThreads (more threads only idled there).
+template <int K, typename WT, typename OT>
+moe_status_t launch_fin_k(const FinArgs& a, cudaStream_t stream) {
+  const int64_t sms = device_info().sm_count;
+  const int64_t one_round = (a.H8 + kChunkUnroll - 1) / kChunkUnroll;  // threads
+  if (one_round > 256 && a.T <= sms)
+    return launch_fin(finalize_kernel<K, WT, OT, 512>, a, stream, 512);
+  if (one_round > kFinThreads && a.T <= 2 * sms)
+    return launch_fin(finalize_kernel<K, WT, OT, 256>, a, stream, 256);
+  return launch_fin(finalize_kernel<K, WT, OT>, a, stream);
 }
 
 using bf16_t = unsigned short;
@@ -185,11 +206,11 @@ using bf16_t = unsigned short;
 // fp32 weights, bf16 output: every specialised K.
 moe_status_t dispatch_default(const FinArgs& a, cudaStream_t stream) {
   switch (a.K) {
-    case 1: return launch_fin(finalize_kernel<1, float, bf16_t>, a, stream);
-    case 2: return launch_fin(finalize_kernel<2, float, bf16_t>, a, stream);
-    case 4: return launch_fin(finalize_kernel<4, float, bf16_t>, a, stream);
-    case 6: return launch_fin(finalize_kernel<6, float, bf16_t>, a, stream);
-    case 8: return launch_fin(finalize_kernel<8, float, bf16_t>, a, stream);
+    case 1: return launch_fin_k<1, float, bf16_t>(a, stream);
+    case 2: return launch_fin_k<2, float, bf16_t>(a, stream);
+    case 4: return launch_fin_k<4, float, bf16_t>(a, stream);
+    case 6: return launch_fin_k<6, float, bf16_t>(a, stream);
+    case 8: return launch_fin_k<8, float, bf16_t>(a, stream);
     default: return launch_fin(finalize_kernel_any_k<float, bf16_t>, a, stream);
   }
 }
@@ -198,8 +219,8 @@ moe_status_t dispatch_default(const FinArgs& a, cudaStream_t stream) {
 template <typename WT, typename OT>
 moe_status_t dispatch_typed(const FinArgs& a, cudaStream_t stream) {
   switch (a.K) {
-    case 2: return launch_fin(finalize_kernel<2, WT, OT>, a, stream);
-    case 8: return launch_fin(finalize_kernel<8, WT, OT>, a, stream);
+    case 2: return launch_fin_k<2, WT, OT>(a, stream);
+    case 8: return launch_fin_k<8, WT, OT>(a, stream);
     default: return launch_fin(finalize_kernel_any_k<WT, OT>, a, stream);
   }
 }

@@ -71,6 +71,18 @@ def test_parity_shapes(K, H):
     assert_finalize_parity(down, restore, w, T, K, H)
 
 
+@pytest.mark.parametrize("K", [2, 8, 3])
+@pytest.mark.parametrize("T", [1, 150, 160, 300, 310, 600, 620])
+def test_parity_across_launch_shapes(T, K):
+    """Token counts on both sides of the launch shape's thresholds (512, 256
+    and 128 threads per token at one, two and more tokens per SM; a fully
+    ordered launch under four tokens per SM), with a ragged last pass of the
+    row (H = 7168 is 896 chunks of 8)."""
+    H = 7168
+    down, restore, w = _case(T, K, H, T * 100 + K)
+    assert_finalize_parity(down, restore, w, T, K, H)
+
+
 def test_permutation_copy():
     """K = 1, weight 1: the output is the unpermuted rows, bit for bit."""
     T, H = 1000, 512
