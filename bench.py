@@ -674,10 +674,11 @@ def run_gpu(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    # Timed region: events only at the step start, before finalize and at the
-    # step end, so the route_index launches (router, rows, scatter; or route
-    # -> create_indices with --separate-index) and finalize chain back to back.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # Timed region: events only at the step start and end, so the route_index
+    # launches (router, rows, scatter; or route -> create_indices with
+    # --separate-index) and finalize chain back to back as a caller runs them
+    # (an event between two launches keeps the second from starting early).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(device_uuid(dev))
     sampler.start()
     time.sleep(0.25)
@@ -689,16 +690,30 @@ def run_gpu(args, cfg, rank, world, local_rank):
         e = ev[i]
         e[0].record(stream)
         pipe.route_and_index(s_d, b_d)
+        pipe.finalize(d_d)
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    # The same K steps again with an event between route + index and
+    # finalize: finalize's own duration in the steps (the roofline) and
+    # route + index's.
+    sev_steps = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        flush_l2()
+        e = sev_steps[i]
+        e[0].record(stream)
+        pipe.route_and_index(s_d, b_d)
         e[1].record(stream)
         pipe.finalize(d_d)
         e[2].record(stream)
     torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - wall0
     clocks = sampler.stop()
 
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    fin_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    fin_ms = [e[1].elapsed_time(e[2]) for e in sev_steps]
+    ri_ms = [e[0].elapsed_time(e[1]) for e in sev_steps]
+    split_step_ms = [e[0].elapsed_time(e[2]) for e in sev_steps]
     mean_step = statistics.fmean(step_ms)
 
     # Per-stage durations (after the timed region): an event between every stage.
@@ -872,6 +887,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": fin_gbs / peak,
                      "frac_vs_nominal_8tbs": fin_gbs / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": nbytes["finalize"],
+                     "timing": "finalize between events in a second pass of the same K timed "
+                               "steps, with an event between route + index and finalize",
                      "traffic": profile_traffic("finalize.cu", "finalize_dsv3_prefill.txt")
                      if cfg.name == "dsv3_prefill" else None},
         "router_roofline": router_roofline(route_gbs, route_mean, peak, nbytes["route"],
@@ -881,14 +898,16 @@ def run_gpu(args, cfg, rank, world, local_rank):
                       "route_index_fused": statistics.fmean(fused_ms),
                       "route_index_single_launch": statistics.fmean(single_ms),
                       "finalize": statistics.fmean(fin_stage_ms),
-                      "route_plus_index_in_timed_steps": statistics.fmean(
-                          [e[0].elapsed_time(e[1]) for e in ev]),
+                      "route_plus_index_in_timed_steps": statistics.fmean(ri_ms),
+                      "step_with_stage_event": statistics.fmean(split_step_ms),
                       "step_median": statistics.median(step_ms),
                       "timed_steps_route_index": "fused" if fused else "separate",
                       "note": "route/create_indices/finalize and route_index_fused from "
                               "separate passes with an event between every stage; the timed "
-                              "steps carry events only at the step start, before finalize and "
-                              "at the step end"},
+                              "steps carry events only at the step start and end; a second "
+                              "pass of the same steps with an event before finalize gives "
+                              "route_plus_index_in_timed_steps, step_with_stage_event and "
+                              "finalize's duration"},
         "next_rows": {"permute": {
             "ms": perm_ms, "tokens_per_s": cfg.T / (perm_ms * 1e-3),
             "achieved_gbs": (2 * cfg.T * cfg.H + 2 * cfg.N * cfg.H + 4 * cfg.N) / (perm_ms * 1e-3) / 1e9,
