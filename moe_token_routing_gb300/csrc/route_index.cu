@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(thread_kernel_warps<EP>() * 32, 1)
 
 // Launches `k` cooperatively with `warps` warps per CTA on min(T /
 // tokens_per_cta, resident CTAs) CTAs, with programmatic stream
-// serialisation when the driver accepts both.
+// serialisation when the CUDA driver accepts both.
 template <typename Kernel>
 moe_status_t launch_fused(Kernel k, FusedArgs f, int warps, int64_t tokens_per_cta, size_t smem,
                           cudaStream_t stream) {

@@ -117,7 +117,7 @@ def test_deterministic():
 @pytest.mark.parametrize("N,E", [(1000, 16), (2048, 256), (131072, 256), (100003, 1000), (0, 8)])
 def test_scales_offsets(N, E):
     """moe_create_indices page, Args scales_offset_p: 128-row aligned offsets
-    of the active experts (the alignment is this build's reading)."""
+    of the active experts (the alignment is the library's reading of the page)."""
     import moe_token_routing_gb300 as moe
     rng = np.random.default_rng(N + E)
     ids = rng.integers(0, E, size=N).astype(np.int32)

@@ -1,5 +1,5 @@
 """Pins for the oracle's aligned scale offsets (moe_create_indices page, Args
-scales_offset_p; the 128-row alignment is this build's reading)."""
+scales_offset_p; the 128-row alignment is the library's reading of the page)."""
 import json
 import os
 
