@@ -983,10 +983,17 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
     p->seg = L;
   // the staged layout: groups of 32 experts, G = 4, 8 or 16, K <= 8, 16-byte
   // loads and bias, a per-element score loader (the softmax loader needs the
-  // whole row's sum and stays on the segment layout)
-  if (S == 32 && (G == 4 || G == 8 || G == 16) && K <= kSegTop && p->vec &&
-      aligned(expert_bias, 16) && score_fn != MOE_SCORES_SOFTMAX)
-    p->staged = G;
+  // whole row's sum and stays on the segment layout). With every group kept
+  // (topk_group == n_groups, e.g. one group) the groups play no part, so E =
+  // 128, 256 or 512 runs there as E/32 units of 32 experts, all kept.
+  const int units = E / 32;
+  const bool unit_shape = units * 32 == E && (units == 4 || units == 8 || units == 16);
+  if (K <= kSegTop && p->vec && aligned(expert_bias, 16) && score_fn != MOE_SCORES_SOFTMAX) {
+    if (S == 32 && (G == 4 || G == 8 || G == 16))
+      p->staged = G;
+    else if (M == G && unit_shape)
+      p->staged = units;
+  }
   return MOE_OK;
 }
 

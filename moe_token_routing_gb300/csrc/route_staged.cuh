@@ -9,7 +9,8 @@
 //
 // Shapes: groups of 32 experts, G = R*P groups (P groups per thread in the
 // first pass), K <= 8, scores as given or through the sigmoid loader, 16-byte
-// aligned scores and bias.
+// aligned scores and bias. With every group kept (topk_group == n_groups)
+// the group size does not matter and G counts units of 32 experts.
 //
 // Data movement. A persistent grid of one CTA per SM splits the token rows
 // into chunks of 32/R rows (contiguous in HBM) and gives each CTA a
@@ -383,7 +384,8 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
 
     // ---- group selection: the M best group scores, ties to the lower group ----
     uint32_t kmask = (G == 32) ? kFullMask : ((1u << G) - 1u);
-    if (a.M < G) {
+    // (with every group kept, G counts units of 32 experts, all kept)
+    if (a.group_mode != kGroupsAllKept && a.M < G) {
       // ahead[i]: groups that beat own group x = hP + i. The other threads'
       // groups are visited by distance d = 1 .. R-1 (thread (h + d) mod R);
       // those of a thread before h have lower indices, so they beat x on an
