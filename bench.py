@@ -58,6 +58,10 @@ def parse_args():
                         "secondary workloads and the host-link windows (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--router-only", action="store_true",
+                   help="launch only the router (moe_route) on the workload's scores, "
+                        "--warmup untimed then --steps timed launches back to back, and "
+                        "print their time (profiling runs of the router at other sizes)")
     return p.parse_args()
 
 
@@ -958,6 +962,43 @@ def run_gpu(args, cfg, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def run_router_only(args, cfg, local_rank):
+    """The router alone on cfg's scores: --warmup untimed launches, then
+    --steps launches back to back between one event pair; prints one JSON
+    line (a profiling aid, not the bench's metric)."""
+    import json as _json
+
+    import torch
+
+    import moe_token_routing_gb300 as moe
+    import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    s_d = torch.from_numpy(synth.make_scores(cfg)).to(dev)
+    b_d = torch.from_numpy(synth.make_bias(cfg)).to(dev)
+    ids = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=dev)
+
+    def call():
+        moe.moe_route(ids, w, s_d, b_d, cfg.G, cfg.M, cfg.norm_weights, cfg.scale)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+    nbytes = 4 * cfg.T * cfg.E + 4 * cfg.E + 8 * cfg.T * cfg.K
+    peak, _ = measured_hbm_peak()
+    print(_json.dumps({"router_only": cfg.name, "tokens": cfg.T, "launches": args.steps,
+                       "us_per_launch": us, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+                       "frac": nbytes / (us * 1e-6) / 1e9 / peak}))
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
@@ -969,6 +1010,9 @@ def main():
         cfg = cfg.replace(T=args.tokens)
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)
+        return
+    if args.router_only:
+        run_router_only(args, cfg, local_rank)
         return
     run_gpu(args, cfg, rank, world, local_rank)
 
