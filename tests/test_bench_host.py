@@ -55,7 +55,10 @@ def test_default_arguments(monkeypatch):
     assert a.warmup >= 3 and not a.separate_index
     monkeypatch.setattr(sys, "argv", ["bench.py", "--separate-index", "--steps", "7"])
     a = bench.parse_args()
-    assert a.separate_index and a.steps == 7
+    assert a.separate_index and a.steps == 7 and not a.router_only
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--router-only", "--tokens", "262144"])
+    a = bench.parse_args()
+    assert a.router_only and a.tokens == 262144
 
 
 def test_router_roofline_headline():
