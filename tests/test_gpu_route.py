@@ -155,6 +155,10 @@ def test_deterministic():
 
 # Segment layout (E = 32 * L, K <= 8, groups of whole lanes): list lengths K < 8,
 # groups spanning several lanes, one group per lane, all groups kept, L = 2 .. 32.
+# The shapes here with every group kept and E = 128, 256 or 512 run on the
+# staged layout instead (units of 32 experts), and so do the near-equal, tie
+# and one-lane cases below for those shapes: both layouts are held to the
+# same exact result.
 SEG_SHAPES = [
     (64, 1, 1, 8), (64, 2, 1, 4), (128, 1, 1, 1), (128, 4, 2, 8), (128, 2, 2, 7),
     (256, 8, 4, 1), (256, 8, 4, 2), (256, 8, 4, 5), (256, 8, 4, 7), (256, 8, 8, 8),
