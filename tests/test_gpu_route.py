@@ -155,7 +155,7 @@ def test_deterministic():
 
 # Segment layout (E = 32 * L, K <= 8, groups of whole lanes): list lengths K < 8,
 # groups spanning several lanes, one group per lane, all groups kept, L = 2 .. 32.
-# The shapes here with every group kept and E = 128, 256 or 512 run on the
+# The shapes here with every group kept and E = 128 or 256 run on the
 # staged layout instead (units of 32 experts), and so do the near-equal, tie
 # and one-lane cases below for those shapes: both layouts are held to the
 # same exact result.
