@@ -56,13 +56,14 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_seg_kernel(const Route
 }
 
 // kKc: K fixed at compile time (8, the common case), or 0 for any K <= 8.
-template <int G, bool kSigmoid, int kKc>
+// kSigmoid / kSoftmax: the score loader (the softmax loader with K = 8 only).
+template <int G, bool kSigmoid, int kKc, bool kSoftmax = false>
 __global__ void __launch_bounds__(kStagedThreadsMax, 1) route_staged_kernel(const RouteArgs a,
                                                                            const StagedSplit sp) {
   extern __shared__ __align__(128) char staged_smem_buf[];
   wait_for_prior_grid();
-  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc>(a, staged_smem_buf, sp,
-                                                              [](int64_t, int, int) {});
+  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc, kSoftmax>(a, staged_smem_buf, sp,
+                                                                        [](int64_t, int, int) {});
 }
 
 template <int EP, bool kVec>
@@ -131,6 +132,10 @@ moe_status_t launch_staged_path_fn(const RoutePlan& p, cudaStream_t stream) {
 
 template <int G>
 moe_status_t launch_staged_path(const RoutePlan& p, cudaStream_t stream) {
+  constexpr int kTok = 32 / kStagedR;
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX)  // K = 8 (plan_route)
+    return launch_staged(route_staged_kernel<G, false, kSegTop, true>, p.a, p.a.T, p.a.E, kTok,
+                         stream);
   if (p.a.score_fn == MOE_SCORES_SIGMOID) return launch_staged_path_fn<G, true>(p, stream);
   return launch_staged_path_fn<G, false>(p, stream);
 }

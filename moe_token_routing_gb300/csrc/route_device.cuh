@@ -982,15 +982,20 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
       (a.group_mode == kGroupsAllKept || (a.group_mode == kGroupsSegment && G <= L && L % G == 0)))
     p->seg = L;
   // the staged layout: groups of 32 experts, G = 4, 8 or 16, K <= 8, 16-byte
-  // loads and bias, a per-element score loader (the softmax loader needs the
-  // whole row's sum and stays on the segment layout). With every group kept
+  // loads and bias, any score loader. The softmax loader takes it with K = 8
+  // and E <= 256 (back to back at 16384 tokens, staged against segment
+  // layout: 15.4 against 18.1 us for the DeepSeek-V3 shape, 10.2 against
+  // 12.9 us for 128 experts all kept) except for 256 experts all kept (17.1
+  // against 16.3 us), which stays on the segment layout. With every group kept
   // (topk_group == n_groups, e.g. one group) the groups play no part, so E =
   // 128 or 256 runs there as E/32 units of 32 experts, all kept (back to back
   // at 16384 tokens: 6.4 against 8.5 us for E = 128 and 9.1 against 9.9 us for
   // E = 256 on the segment layout; E = 512, 20.7 against 17.7 us, stays there).
   const int units = E / 32;
   const bool unit_shape = units * 32 == E && (units == 4 || units == 8);
-  if (K <= kSegTop && p->vec && aligned(expert_bias, 16) && score_fn != MOE_SCORES_SOFTMAX) {
+  const bool softmax_ok = K == kSegTop && E <= 256 && !(M == G && E == 256);
+  if (K <= kSegTop && p->vec && aligned(expert_bias, 16) &&
+      (score_fn != MOE_SCORES_SOFTMAX || softmax_ok)) {
     if (S == 32 && (G == 4 || G == 8 || G == 16))
       p->staged = G;
     else if (M == G && unit_shape)

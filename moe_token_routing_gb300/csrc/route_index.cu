@@ -564,7 +564,8 @@ __global__ void __launch_bounds__(kRouteThreads, 3) route_count_seg_kernel(const
 }
 
 // kKc: K fixed at compile time (8, the common case), or 0 for any K <= 8.
-template <int G, bool kSigmoid, int kKc>
+// kSigmoid / kSoftmax: the score loader (the softmax loader with K = 8 only).
+template <int G, bool kSigmoid, int kKc, bool kSoftmax = false>
 __global__ void __launch_bounds__(kStagedThreadsMax, 1)
     route_count_staged_kernel(const CountRouteArgs c, const StagedSplit sp) {
   extern __shared__ __align__(128) char staged_smem_buf[];
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kStagedThreadsMax, 1)
   uint32_t* const counts = c.counts;
   const int row = c.row, E = c.r.E;
   const int64_t K = c.r.K;
-  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc>(
+  route_tokens_staged<kStagedR, G / kStagedR, kSigmoid, kKc, kSoftmax>(
       c.r, staged_smem_buf, sp,
       [=](int64_t t, int k, int id) { count_slot(counts, row, E, t * K + k, id); });
 }
@@ -684,6 +685,10 @@ moe_status_t launch_count_staged_fn(const CountRouteArgs& c, cudaStream_t stream
 template <int G>
 moe_status_t launch_count_staged(const RoutePlan& p, const CountRouteArgs& c,
                                  cudaStream_t stream) {
+  constexpr int kTok = 32 / kStagedR;
+  if (p.a.score_fn == MOE_SCORES_SOFTMAX)  // K = 8 (plan_route)
+    return launch_staged(route_count_staged_kernel<G, false, kSegTop, true>, c, c.r.T, c.r.E,
+                         kTok, stream);
   if (p.a.score_fn == MOE_SCORES_SIGMOID) return launch_count_staged_fn<G, true>(c, stream);
   return launch_count_staged_fn<G, false>(c, stream);
 }

@@ -233,11 +233,12 @@ __device__ __forceinline__ uint32_t score_order_key(float v) { return ordered_ke
 // thread of the CTA calls it. `smem` is the CTA's dynamic shared memory in the
 // staged_smem(E, 32/R, W, D) layout. After token t's ids and weights are
 // written, on_id(t, k, id) is called once per k < K.
-template <int R, int P, bool kSigmoid, int kKc, typename OnId>
+template <int R, int P, bool kSigmoid, int kKc, bool kSoftmax, typename OnId>
 __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* smem,
                                                     const StagedSplit& sp, OnId on_id) {
   const int D = sp.depth;
   static_assert(R == 2 || R == 4, "two or four threads per token");
+  static_assert(!(kSigmoid && kSoftmax), "one score loader");
   static_assert(kKc >= 0 && kKc <= kSegTop, "K fixed at compile time (1 .. 8) or 0");
   const int K = kKc > 0 ? kKc : a.K;  // experts per token
   constexpr int G = R * P;
@@ -340,6 +341,55 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     const bool live = t < a.T;
     float* row = ring + (size_t)s * kRow + tq * E;
 
+    // ---- softmax loader: the row's max, exp(x - max) over the row, and the
+    // fp32 sum of those in ascending expert order (thread h's experts follow
+    // those of threads 0 .. h-1, so the running sum passes from thread to
+    // thread); pass 1 divides by it ----
+    float ssum = 1.0f;
+    if constexpr (kSoftmax) {
+      float m = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        const float* rg = row + (h * P + i) * 32;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 v = *reinterpret_cast<const float4*>(rg + ((c + rot) & 7) * 4);
+          m = fmaxf(fmaxf(m, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < R; off <<= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        float* rg = row + (h * P + i) * 32;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float4* q = reinterpret_cast<float4*>(rg + ((c + rot) & 7) * 4);
+          const float4 v = *q;
+          const float4 e = make_float4(score_exp_f32(__fsub_rn(v.x, m)), score_exp_f32(__fsub_rn(v.y, m)),
+                                       score_exp_f32(__fsub_rn(v.z, m)), score_exp_f32(__fsub_rn(v.w, m)));
+          if (live) *q = e;
+        }
+      }
+      float run = 0.0f;
+#pragma unroll
+      for (int l = 0; l < R; ++l) {
+        if (h == l) {
+#pragma unroll
+          for (int i = 0; i < P; ++i) {
+            const float* rg = row + (h * P + i) * 32;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float4 e = *reinterpret_cast<const float4*>(rg + c * 4);
+              run = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(run, e.x), e.y), e.z), e.w);
+            }
+          }
+        }
+        run = __shfl_sync(kFullMask, run, tbase + l);
+      }
+      ssum = run;
+    }
+
     // ---- pass 1: scores of this thread's P groups (top-2 of each float4 by
     // two min/max pairs, then the eight float4 top-2s merged as a tree, so the
     // merges of a group form three dependent levels rather than a chain) ----
@@ -358,6 +408,11 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
         if constexpr (kSigmoid) {
           v = make_float4(sigmoid_score(v.x), sigmoid_score(v.y), sigmoid_score(v.z),
                           sigmoid_score(v.w));
+          if (live) *reinterpret_cast<float4*>(rg + col) = v;  // pass 2 and the weights read it
+        }
+        if constexpr (kSoftmax) {
+          v = make_float4(__fdiv_rn(v.x, ssum), __fdiv_rn(v.y, ssum), __fdiv_rn(v.z, ssum),
+                          __fdiv_rn(v.w, ssum));
           if (live) *reinterpret_cast<float4*>(rg + col) = v;  // pass 2 and the weights read it
         }
         const float4 bb = *reinterpret_cast<const float4*>(bg + col);
@@ -380,7 +435,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
       gk[i] = score_order_key(__fadd_rn(q1[0], q2[0]));
       sec[i] = q2[0];
     }
-    if constexpr (kSigmoid) __syncwarp();
+    if constexpr (kSigmoid || kSoftmax) __syncwarp();
 
     // ---- group selection: the M best group scores, ties to the lower group ----
     uint32_t kmask = (G == 32) ? kFullMask : ((1u << G) - 1u);
@@ -611,7 +666,9 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     while (pending) {
       const int l0 = __ffs(pending) - 1;
       pending &= pending - 1;
-      route_one_token_exact<E / 32, false>(a, t - tq + l0 / R, nullptr, on_id);
+      // (the softmax loader's strip: this warp's ring buffer, whose chunk is done)
+      route_one_token_exact<E / 32, kSoftmax>(a, t - tq + l0 / R,
+                                              kSoftmax ? ring + (size_t)s * kRow : nullptr, on_id);
     }
 
     // ---- the buffer is free: start the copy of this warp's chunk D ahead ----
