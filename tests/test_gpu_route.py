@@ -294,7 +294,8 @@ def test_softmax_loader_on_workloads(name):
 @pytest.mark.parametrize("E,G,M,K", [(8, 4, 2, 3), (12, 3, 2, 4), (32, 4, 2, 8), (48, 4, 2, 6),
                                      (96, 4, 2, 8), (120, 5, 2, 8), (256, 8, 4, 8),
                                      (384, 1, 1, 8), (1024, 32, 4, 8),
-                                     # segment layout: L = 2, 4, 8, 16 lanes per token, K < 8
+                                     # segment layout: L = 2, 4, 8, 16 lanes per token, K < 8;
+                                     # (256, 8, 4, 8) and (128, 1, 1, 8) take the staged one
                                      (64, 2, 1, 4), (128, 1, 1, 8), (256, 8, 4, 3),
                                      (512, 16, 4, 8)])
 @pytest.mark.parametrize("norm", [True, False])
