@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_index_workspace_size.restype = sz
     lib.moe_route_index_single_launch_workspace_size.argtypes = [i64, i32]
     lib.moe_route_index_single_launch_workspace_size.restype = sz
+    lib.moe_create_indices_no_alloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, vp, vp]
+    lib.moe_create_indices_no_alloc.restype = ctypes.c_int
     for fn in (lib.moe_route_index, lib.moe_route_index_single_launch):
         fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32,
                        ctypes.c_int, vp, sz, vp, vp]
@@ -305,11 +307,7 @@ def moe_create_indices_no_alloc(token_expert_order: torch.Tensor,
     (see include/moe_routing.h for its size limit and sharing rules).
     device_status, if given, is a 1-element int32 CUDA tensor that receives
     the device status word."""
-    lib = load_library()
-    f = lib.moe_create_indices_no_alloc
-    vp = ctypes.c_void_p
-    f.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
-    f.restype = ctypes.c_int
+    f = load_library().moe_create_indices_no_alloc
     N = topk_ids.numel()
     E = expert_ids.numel()
     args = (_dev(token_expert_order, "token_expert_order", torch.int32, (N,)),
