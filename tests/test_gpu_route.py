@@ -312,6 +312,29 @@ def test_softmax_loader_shapes_and_extremes(E, G, M, K, norm):
     assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("fn", ["sigmoid", "softmax"])
+@pytest.mark.parametrize("E,G,M,K", [(128, 4, 2, 8), (256, 8, 4, 8), (512, 16, 4, 8),
+                                     (128, 1, 1, 8), (256, 1, 1, 8), (256, 8, 4, 6)])
+def test_loader_tie_stress(fn, E, G, M, K):
+    """Gate logits on a grid of five values, so that dozens of a row's loaded
+    scores are equal: ties in the biased scores, the group scores and the
+    group ranks. The staged layout (groups or units of 32 experts; softmax
+    with K = 8 and at most 256 experts) ranks them by exact keys or hands
+    the token to the exact path, which for softmax rebuilds the row; the
+    result must still be the oracle's, bit for bit."""
+    rng = np.random.default_rng(E + 10 * K + len(fn))
+    T = 515
+    logits = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    load = oracle.sigmoid if fn == "sigmoid" else oracle.softmax
+    run = gpu_route_sigmoid if fn == "sigmoid" else gpu_route_softmax
+    for bias in (np.zeros(E, np.float32), (rng.integers(-1, 2, size=E) / 8).astype(np.float32)):
+        ids_ref, w_ref = oracle.route(load(logits), bias, K, G, M, True, 2.5)
+        ids, w = run(logits, bias, K, G, M, True, 2.5)
+        bad = np.nonzero((ids != ids_ref).any(axis=1))[0]
+        assert bad.size == 0, f"{bad.size} rows differ, first token {bad[:1]}"
+        assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))
+
+
 def _mbar_selftest_lib():
     """The bounded-wait harness of tests/cuda (the staged router's chunk wait),
     built with nvcc for sm_103a."""

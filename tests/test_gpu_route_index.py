@@ -329,6 +329,26 @@ def test_fused_pipeline_matches_separate_launches():
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
 
 
+@pytest.mark.parametrize("fn", ["sigmoid", "softmax"])
+@pytest.mark.parametrize("E,G,M", [(256, 8, 4), (128, 1, 1)])
+def test_loader_tie_stress(fn, E, G, M):
+    """Gate logits on a grid of five values (dozens of equal scores per row)
+    through the counting router's loaders: the tokens that the tie ranking
+    or the exact path settle are counted like the others."""
+    rng = np.random.default_rng(E + len(fn))
+    T, K = 515, 8
+    logits = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    bias = np.zeros(E, np.float32)
+    load = oracle.sigmoid if fn == "sigmoid" else oracle.softmax
+    ids_ref, w_ref = oracle.route(load(logits), bias, K, G, M, True, 2.5)
+    idx_ref = oracle.create_indices(ids_ref, E)
+    moe = _moe()
+    code = moe.SCORES_SIGMOID if fn == "sigmoid" else moe.SCORES_SOFTMAX
+    got, bufs = gpu_route_index(logits, bias, K, G, M, True, 2.5, score_fn=code)
+    assert_parity(got, ids_ref, w_ref, idx_ref, E)
+    assert bufs.device_status() == 0
+
+
 @BOTH
 @pytest.mark.parametrize("name", ["dsv3_decode", "skewed_ungrouped", "few_expert_large_batch"])
 def test_softmax_loader(name, single):
