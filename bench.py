@@ -491,6 +491,69 @@ def host_link_evidence(streamer, pipe, s_h, b_h, down_h, outs_h):
                 "compute; 20 more e2e steps"}
 
 
+READ_FLOOR_SHAPES = [(152 * m, b) for m in (1, 2, 4, 8) for b in (256, 512)]
+
+
+def pick_read_floor(times: dict):
+    """The fastest (grid, block) of a sweep {shape: us per launch, or None};
+    None when no shape was timed."""
+    timed = {k: v for k, v in times.items() if v is not None}
+    if not timed:
+        return None
+    best = min(timed, key=timed.get)
+    return best, timed[best]
+
+
+def streaming_read_floor(bufs, n: int, dev, peak):
+    """What one launch that only reads the score bytes costs: the bench's
+    streaming-read kernel (bench_read_floor.cu: 16-byte loads at a grid
+    stride, summed in registers, one partial sum per CTA) over the same
+    rotating score copies, captured in a CUDA graph and replayed like the
+    router, at the fastest of a few grid and block sizes. Its per-CTA sums are
+    checked against torch.sum of the same buffer, so the timed kernel is known
+    to read every word. None when the kernel was not built."""
+    import ctypes
+
+    import torch
+    path = os.path.join(ROOT, "bench_read_floor.so")
+    if not os.path.exists(path):
+        return {"note": "bench_read_floor.so not built (__graft_entry__.build builds it)"}
+    lib = ctypes.CDLL(path)
+    lib.read_floor_launch.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.read_floor_launch.restype = ctypes.c_int
+    n4 = bufs[0].numel() // 4
+    nbytes = 16 * n4
+    partial = torch.zeros(max(g for g, _ in READ_FLOOR_SHAPES), dtype=torch.float32, device=dev)
+    ptrs = [b.data_ptr() for b in bufs]
+
+    def launcher(grid, block):
+        def call(i, st):
+            rc = lib.read_floor_launch(ptrs[i % len(ptrs)], n4, partial.data_ptr(), grid, block,
+                                       st.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(f"read_floor_launch failed: {rc}")
+        return call
+
+    times = {shape: time_graph_replay(launcher(*shape), n, dev) for shape in READ_FLOOR_SHAPES}
+    pick = pick_read_floor(times)
+    if pick is None:
+        return {"note": "graph capture failed"}
+    (grid, block), us = pick
+    # the check: one launch on buffer 0 at the chosen shape
+    s = torch.cuda.current_stream(dev)
+    partial.zero_()
+    launcher(grid, block)(0, s)
+    torch.cuda.synchronize(dev)
+    got = float(partial[:grid].double().sum())
+    want = float(bufs[0].double().sum())
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_launch": us, "achieved_gbs": gbs, "frac": gbs / peak,
+            "shape": f"{grid} CTAs x {block} threads",
+            "sweep_us": {f"{g}x{b}": t for (g, b), t in times.items()},
+            "sum_rel_err": abs(got - want) / max(abs(want), 1e-30)}
+
+
 def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     """The router alone, launched back to back: on the workload's batch
     rotating over copies whose total exceeds L2 twice over, on a 262144-token
@@ -539,6 +602,7 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
     def read_fn(i, st=None):
         torch.sum(bufs[i % len(bufs)], dim=1, out=acc)
     read_graph = time_graph_replay(read_fn, n, dev)
+    stream_read = streaming_read_floor(bufs, n, dev, peak)
     del bufs
     big_T = 262144
     big = torch.from_numpy(synth.make_scores(cfg.replace(T=big_T))).to(dev)
@@ -584,7 +648,12 @@ def router_evidence(moe, cfg, s_d, b_d, dev, stream, peak):
             "back_to_back": graph_entry(graph_b2b, rb),
             "large_batch": graph_entry(big_graph, bb),
             "launch_floor_us": floor_graph,
-            "read_only_kernel": graph_entry(read_graph, 4 * T * E)},
+            "read_only_kernel": graph_entry(read_graph, 4 * T * E),
+            "streaming_read": stream_read},
+        "one_launch_read_ceiling": (
+            {"us_per_launch": stream_read["us_per_launch"], "frac": stream_read["frac"],
+             "note": "graph_replay.streaming_read: a launch that only reads these bytes"}
+            if "frac" in stream_read else None),
         "hbm_time_at_peak_us": rb / (peak * 1e3),
         "residue_over_hbm_time_us": b2b - rb / (peak * 1e3),
     }

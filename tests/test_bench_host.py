@@ -74,3 +74,34 @@ def test_router_roofline_headline():
     r = bench.router_roofline(1500.0, 0.012, 6787.6, 17826816, None)
     assert r["achieved"] == 1500.0
     assert r["timing"] == r["single_launch"]["timing"]
+
+
+def test_read_floor_pick_and_shapes():
+    """The streaming-read floor takes the fastest timed shape of its sweep; the
+    shapes are whole multiples of the 152 SMs with block sizes the kernel
+    accepts (a multiple of 32, at most 512)."""
+    import bench
+    assert bench.pick_read_floor({(152, 256): 5.0, (304, 512): 4.6, (608, 256): None}) == \
+        ((304, 512), 4.6)
+    assert bench.pick_read_floor({(152, 256): None}) is None
+    for grid, block in bench.READ_FLOOR_SHAPES:
+        assert grid % 152 == 0 and block % 32 == 0 and 32 <= block <= 512
+
+
+def test_read_floor_kernel_is_built_for_sm_103a():
+    """build() compiles the bench's streaming-read kernel and its launcher
+    rejects shapes outside what the kernel handles without launching."""
+    import ctypes
+    import shutil
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("no nvcc")
+    import __graft_entry__ as g
+    path = g.build_read_floor()
+    lib = ctypes.CDLL(path)
+    lib.read_floor_launch.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.read_floor_launch.restype = ctypes.c_int
+    # argument checks happen before any CUDA call
+    assert lib.read_floor_launch(None, 4, 16, 152, 256, None) == -1
+    assert lib.read_floor_launch(16, 4, 16, 152, 1024, None) == -1
+    assert lib.read_floor_launch(18, 4, 16, 152, 256, None) == -1
