@@ -1,0 +1,171 @@
+"""Parity past 2^31 elements: the router on a score matrix, finalize on a
+`down` matrix and permute on an output of more than 2^31 elements, so that
+every offset into them needs 64-bit arithmetic. The oracle checks sampled
+rows (the first ones, those on both sides of element 2^31, the last ones and
+random ones) one by one; the index build on the router's 69 million slots is
+checked against the definitions of its outputs (inverse permutation, stable
+order within each expert, counts, compact CSR, stats) on the whole arrays.
+
+Inputs come from torch's seeded generator on the device (uniform scores,
+normal `down`, a random permutation as the restore order); the sampled rows
+are copied to the host for the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _guard import check_all, guarded
+from _workloads import f32_to_bf16_bits, finalize_tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+TWO31 = 1 << 31
+
+
+def _moe():
+    import moe_token_routing_gb300 as moe
+    moe.load_library()
+    return moe
+
+
+def _sample_rows(n_rows, boundary_row, seed, k=300, n_random=1000):
+    rng = np.random.default_rng(seed)
+    parts = [np.arange(0, k), np.arange(boundary_row - k, boundary_row + k),
+             np.arange(n_rows - k, n_rows), rng.integers(0, n_rows, n_random)]
+    return np.unique(np.concatenate(parts).clip(0, n_rows - 1))
+
+
+def _free():
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def test_router_and_index_past_2_31_score_elements():
+    """DeepSeek-V3 router shape (256 experts in 8 groups, top-4 groups, K = 8)
+    on 8.65 million tokens: 2.2 billion scores (8.9 GB), a ragged last chunk,
+    thousands of ring buffer turns per warp."""
+    moe = _moe()
+    E, G, M, K = 256, 8, 4, 8
+    boundary = TWO31 // E
+    T = boundary + 262144 + 3
+    gen = torch.Generator(device="cuda").manual_seed(20231)
+    s = torch.rand((T, E), generator=gen, device="cuda", dtype=torch.float32)
+    bias = torch.randn(E, generator=gen, device="cuda", dtype=torch.float32) * 0.05
+    ids, gi = guarded((T, K), torch.int32, name="expert_indices")
+    w, gw = guarded((T, K), torch.float32, name="expert_weights")
+    moe.moe_route(ids, w, s, bias, G, M, True, 2.5)
+    check_all([gi, gw])
+
+    rows = _sample_rows(T, boundary, 1)
+    sel = torch.from_numpy(rows).cuda()
+    ids_ref, w_ref = oracle.route(s.index_select(0, sel).cpu().numpy(), bias.cpu().numpy(),
+                                  K, G, M, True, 2.5)
+    got_ids = ids.index_select(0, sel).cpu().numpy()
+    bad = np.nonzero((got_ids != ids_ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} sampled rows differ, first token {rows[bad[:1]]}"
+    assert np.array_equal(w.index_select(0, sel).cpu().numpy().view(np.uint32),
+                          w_ref.view(np.uint32))
+
+    # the same router counting its own output, then the index build over
+    # N = T*K = 69 million slots
+    N = T * K
+    bufs = moe.RouteIndexBuffers(T, E, K, "cuda")
+    bufs.run(s, bias, G, M, True, 2.5)
+    del s
+    _free()
+    assert bufs.device_status() == 0
+    assert torch.equal(bufs.expert_indices, ids)
+    assert torch.equal(bufs.expert_weights.view(torch.int32), w.view(torch.int32))
+    flat = ids.reshape(-1).long()
+    del ids, w, gi, gw
+    _free()
+    order = bufs.token_expert_order.long()
+    restore = bufs.restore_token_order.long()
+    # restore_token_order is the inverse permutation of token_expert_order
+    assert torch.equal(order[restore], torch.arange(N, device="cuda"))
+    del restore
+    _free()
+    # experts ascend along the order, and slots ascend within each expert
+    e_sorted = flat[order]
+    assert bool((e_sorted[1:] >= e_sorted[:-1]).all())
+    same = e_sorted[1:] == e_sorted[:-1]
+    assert bool((order[1:] > order[:-1])[same].all())
+    del order, same
+    _free()
+    # compact CSR over the active experts, expert_ids, stats
+    counts = torch.bincount(flat, minlength=E)
+    active = torch.nonzero(counts).reshape(-1)
+    A = active.numel()
+    starts = torch.cat([torch.zeros(1, dtype=torch.long, device="cuda"),
+                        torch.cumsum(counts[active], 0)])
+    csr = bufs.expert_start_indices.long()
+    assert torch.equal(csr[:A + 1], starts)
+    assert bool((csr[A + 1:] == N).all())
+    eids = bufs.expert_ids.long()
+    assert torch.equal(eids[:A], active)
+    assert bool((eids[A:] == -1).all())
+    assert bufs.expert_usage_stats.cpu().tolist() == [int(counts.max()), A]
+    # the flat order sorted by expert agrees with the sorted ids
+    assert torch.equal(e_sorted, torch.sort(flat).values)
+    del bufs, flat, e_sorted
+    _free()
+
+
+def test_finalize_past_2_31_down_elements():
+    """The prefill row width (H = 7168) and K = 8 over 40 000 tokens: `down`
+    holds 2.29 billion bf16 values (4.6 GB), and the restore order is a random
+    permutation, so sampled tokens gather rows on both sides of element 2^31."""
+    moe = _moe()
+    T, K, H = 40000, 8, 7168
+    N = T * K
+    assert N * H > TWO31
+    gen = torch.Generator(device="cuda").manual_seed(20232)
+    down = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, N, 32768):
+        r1 = min(N, r0 + 32768)
+        down[r0:r1] = torch.randn((r1 - r0, H), generator=gen, device="cuda").to(torch.bfloat16)
+    restore = torch.randperm(N, generator=gen, device="cuda").to(torch.int32)
+    w = torch.rand((T, K), generator=gen, device="cuda", dtype=torch.float32) * 2 - 0.5
+    out, g = guarded((T, H), torch.bfloat16, name="output")
+    moe.moe_finalize(out, down, restore, w)
+    check_all([g])
+
+    # tokens whose rows lie past element 2^31 among the sampled ones
+    far_row = TWO31 // H
+    tok = _sample_rows(T, T // 2, 2)
+    r_s = restore.reshape(T, K)[torch.from_numpy(tok).cuda()].long()
+    assert int((r_s >= far_row).sum()) > 0
+    # the oracle on the sampled tokens: their K rows gathered in order, so
+    # that token j of the sample reads rows j*K .. j*K+K-1
+    rows_c = down.index_select(0, r_s.reshape(-1)).view(torch.int16).cpu().numpy().view(np.uint16)
+    S = tok.size
+    w_c = w[torch.from_numpy(tok).cuda()].cpu().numpy()
+    ref = oracle.finalize(rows_c, np.arange(S * K, dtype=np.uint32), w_c, S, K, H)
+    got = out[torch.from_numpy(tok).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    ok = finalize_tolerance_ok(got, ref)
+    assert ok.all(), f"{(~ok).sum()} elements outside 1e-2 + 8e-3|ref|"
+    assert np.array_equal(got, f32_to_bf16_bits(ref))
+    del down, restore, w, out, g
+    _free()
+
+
+def test_permute_past_2_31_output_elements():
+    """permuted[restore[t*K + k]] = input[t] with T*K*H above 2^31 (the prefill
+    row width, K = 8, 40 000 tokens), checked on every slot."""
+    moe = _moe()
+    T, K, H = 40000, 8, 7168
+    N = T * K
+    gen = torch.Generator(device="cuda").manual_seed(20233)
+    x = torch.randn((T, H), generator=gen, device="cuda").to(torch.bfloat16)
+    restore = torch.randperm(N, generator=gen, device="cuda").to(torch.int32)
+    out, g = guarded((N, H), torch.bfloat16, name="permuted")
+    moe.moe_permute(out, x, restore)
+    check_all([g])
+    src = torch.arange(N, device="cuda") // K
+    r = restore.long()
+    for i0 in range(0, N, 65536):
+        i1 = min(N, i0 + 65536)
+        assert torch.equal(out[r[i0:i1]].view(torch.int16), x[src[i0:i1]].view(torch.int16)), i0
+    del x, restore, out, g, src, r
+    _free()
