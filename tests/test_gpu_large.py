@@ -2,8 +2,8 @@
 `down` matrix and permute on an output of more than 2^31 elements, so that
 every offset into them needs 64-bit arithmetic. The oracle checks sampled
 rows (the first ones, those on both sides of element 2^31, the last ones and
-random ones) one by one; the index build on the router's 69 million slots is
-checked against the definitions of its outputs (inverse permutation, stable
+random ones) one by one; the index build on the router's slots (up to 135
+million) is checked against the definitions of its outputs (inverse permutation, stable
 order within each expert, counts, compact CSR, stats) on the whole arrays.
 
 Inputs come from torch's seeded generator on the device (uniform scores,
@@ -41,15 +41,20 @@ def _free():
     torch.cuda.empty_cache()
 
 
-def test_router_and_index_past_2_31_score_elements():
-    """DeepSeek-V3 router shape (256 experts in 8 groups, top-4 groups, K = 8)
-    on 8.65 million tokens: 2.2 billion scores (8.9 GB), a ragged last chunk,
-    thousands of ring buffer turns per warp."""
+@pytest.mark.parametrize("E,G,M,K", [(256, 8, 4, 8), (1024, 32, 4, 8), (200, 8, 4, 6),
+                                     (32, 4, 2, 2)],
+                         ids=["staged", "segment", "warp", "thread"])
+def test_router_and_index_past_2_31_score_elements(E, G, M, K):
+    """More than 2^31 scores (about 8.9 GB) in each router layout: the
+    DeepSeek-V3 shape (256 experts in 8 groups, top-4 groups, K = 8; 8.65
+    million tokens, a ragged last chunk, thousands of ring buffer turns per
+    warp), 1024 experts in 32 groups (segment layout), 200 experts in 8
+    groups of 25 (warp layout) and 32 experts in 4 groups (thread layout, 67
+    million tokens)."""
     moe = _moe()
-    E, G, M, K = 256, 8, 4, 8
     boundary = TWO31 // E
     T = boundary + 262144 + 3
-    gen = torch.Generator(device="cuda").manual_seed(20231)
+    gen = torch.Generator(device="cuda").manual_seed(20231 + E)
     s = torch.rand((T, E), generator=gen, device="cuda", dtype=torch.float32)
     bias = torch.randn(E, generator=gen, device="cuda", dtype=torch.float32) * 0.05
     ids, gi = guarded((T, K), torch.int32, name="expert_indices")
@@ -57,7 +62,7 @@ def test_router_and_index_past_2_31_score_elements():
     moe.moe_route(ids, w, s, bias, G, M, True, 2.5)
     check_all([gi, gw])
 
-    rows = _sample_rows(T, boundary, 1)
+    rows = _sample_rows(T, boundary, E)
     sel = torch.from_numpy(rows).cuda()
     ids_ref, w_ref = oracle.route(s.index_select(0, sel).cpu().numpy(), bias.cpu().numpy(),
                                   K, G, M, True, 2.5)
@@ -68,7 +73,7 @@ def test_router_and_index_past_2_31_score_elements():
                           w_ref.view(np.uint32))
 
     # the same router counting its own output, then the index build over
-    # N = T*K = 69 million slots
+    # N = T*K slots (17 to 135 million)
     N = T * K
     bufs = moe.RouteIndexBuffers(T, E, K, "cuda")
     bufs.run(s, bias, G, M, True, 2.5)
