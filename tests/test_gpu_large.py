@@ -74,7 +74,6 @@ def test_router_and_index_past_2_31_score_elements(E, G, M, K):
 
     # the same router counting its own output, then the index build over
     # N = T*K slots (17 to 135 million)
-    N = T * K
     bufs = moe.RouteIndexBuffers(T, E, K, "cuda")
     bufs.run(s, bias, G, M, True, 2.5)
     del s
@@ -85,6 +84,15 @@ def test_router_and_index_past_2_31_score_elements(E, G, M, K):
     flat = ids.reshape(-1).long()
     del ids, w, gi, gw
     _free()
+    _check_index(bufs, flat, E)
+    del bufs, flat
+    _free()
+
+
+def _check_index(bufs, flat, E):
+    """The index outputs in `bufs` against their definitions for the flat
+    expert ids `flat` (int64 on the device), on the whole arrays."""
+    N = flat.numel()
     order = bufs.token_expert_order.long()
     restore = bufs.restore_token_order.long()
     # restore_token_order is the inverse permutation of token_expert_order
@@ -97,6 +105,10 @@ def test_router_and_index_past_2_31_score_elements(E, G, M, K):
     same = e_sorted[1:] == e_sorted[:-1]
     assert bool((order[1:] > order[:-1])[same].all())
     del order, same
+    _free()
+    # the order's experts are the sorted ids
+    assert torch.equal(e_sorted, torch.sort(flat).values)
+    del e_sorted
     _free()
     # compact CSR over the active experts, expert_ids, stats
     counts = torch.bincount(flat, minlength=E)
@@ -111,9 +123,54 @@ def test_router_and_index_past_2_31_score_elements(E, G, M, K):
     assert torch.equal(eids[:A], active)
     assert bool((eids[A:] == -1).all())
     assert bufs.expert_usage_stats.cpu().tolist() == [int(counts.max()), A]
-    # the flat order sorted by expert agrees with the sorted ids
-    assert torch.equal(e_sorted, torch.sort(flat).values)
-    del bufs, flat, e_sorted
+
+
+def test_create_indices_on_134_million_slots():
+    """The separate index build (count, rows and scatter kernels) on 2^27 + 5
+    slots over 256 experts, ids from a skewed draw (expert e with weight
+    proportional to e + 1), against the definitions of its outputs."""
+    moe = _moe()
+    E, N = 256, (1 << 27) + 5
+    gen = torch.Generator(device="cuda").manual_seed(20234)
+    p = torch.arange(1, E + 1, dtype=torch.float32, device="cuda")
+    ids = torch.multinomial(p, 1 << 20, replacement=True, generator=gen).to(torch.int32)
+    reps = -(-N // ids.numel())
+    perm = torch.randperm(ids.numel() * reps, generator=gen, device="cuda")
+    flat_ids = ids.repeat(reps)[perm][:N].contiguous()
+    del perm
+    bufs = moe.create_indices(flat_ids, E)
+    assert bufs.device_status() == 0
+    _check_index(bufs, flat_ids.long(), E)
+    del bufs, flat_ids, ids
+    _free()
+
+
+def test_single_launch_route_index_past_2_31_score_elements():
+    """The cooperative single-launch router + index on the DeepSeek-V3 shape
+    over 8.65 million tokens (more than 2^31 scores): the same ids and weights
+    as moe_route on sampled rows' oracle results, and index outputs that meet
+    their definitions."""
+    moe = _moe()
+    E, G, M, K = 256, 8, 4, 8
+    boundary = TWO31 // E
+    T = boundary + 262144 + 3
+    gen = torch.Generator(device="cuda").manual_seed(20235)
+    s = torch.rand((T, E), generator=gen, device="cuda", dtype=torch.float32)
+    bias = torch.randn(E, generator=gen, device="cuda", dtype=torch.float32) * 0.05
+    bufs = moe.RouteIndexBuffers(T, E, K, "cuda", single_launch=True)
+    bufs.run(s, bias, G, M, True, 2.5)
+    assert bufs.device_status() == 0
+    rows = _sample_rows(T, boundary, 3)
+    sel = torch.from_numpy(rows).cuda()
+    ids_ref, w_ref = oracle.route(s.index_select(0, sel).cpu().numpy(), bias.cpu().numpy(),
+                                  K, G, M, True, 2.5)
+    del s
+    _free()
+    assert np.array_equal(bufs.expert_indices.index_select(0, sel).cpu().numpy(), ids_ref)
+    assert np.array_equal(bufs.expert_weights.index_select(0, sel).cpu().numpy().view(np.uint32),
+                          w_ref.view(np.uint32))
+    _check_index(bufs, bufs.expert_indices.reshape(-1).long(), E)
+    del bufs
     _free()
 
 
