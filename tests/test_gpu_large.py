@@ -174,12 +174,43 @@ def test_single_launch_route_index_past_2_31_score_elements():
     _free()
 
 
-def test_finalize_past_2_31_down_elements():
-    """The prefill row width (H = 7168) and K = 8 over 40 000 tokens: `down`
-    holds 2.29 billion bf16 values (4.6 GB), and the restore order is a random
+@pytest.mark.parametrize("fn", ["sigmoid", "softmax"])
+def test_score_loaders_past_2_31_logits(fn):
+    """The fused sigmoid and softmax loaders on the DeepSeek-V3 router shape
+    over 8.65 million tokens of gate logits (more than 2^31 of them), sampled
+    rows against the oracle's loader followed by its router."""
+    moe = _moe()
+    E, G, M, K = 256, 8, 4, 8
+    boundary = TWO31 // E
+    T = boundary + 262144 + 3
+    gen = torch.Generator(device="cuda").manual_seed(20236 + len(fn))
+    x = torch.randn((T, E), generator=gen, device="cuda", dtype=torch.float32)
+    bias = torch.randn(E, generator=gen, device="cuda", dtype=torch.float32) * 0.05
+    ids, gi = guarded((T, K), torch.int32, name="expert_indices")
+    w, gw = guarded((T, K), torch.float32, name="expert_weights")
+    code = moe.SCORES_SIGMOID if fn == "sigmoid" else moe.SCORES_SOFTMAX
+    moe.moe_route_ex(ids, w, x, bias, G, M, True, 2.5, code)
+    check_all([gi, gw])
+    rows = _sample_rows(T, boundary, 4 + len(fn))
+    sel = torch.from_numpy(rows).cuda()
+    load = oracle.sigmoid if fn == "sigmoid" else oracle.softmax
+    ids_ref, w_ref = oracle.route(load(x.index_select(0, sel).cpu().numpy()), bias.cpu().numpy(),
+                                  K, G, M, True, 2.5)
+    assert np.array_equal(ids.index_select(0, sel).cpu().numpy(), ids_ref)
+    assert np.array_equal(w.index_select(0, sel).cpu().numpy().view(np.uint32),
+                          w_ref.view(np.uint32))
+    del x, ids, w, gi, gw
+    _free()
+
+
+@pytest.mark.parametrize("K", [8, 16])
+def test_finalize_past_2_31_down_elements(K):
+    """The prefill row width (H = 7168) over 320 000 slots (40 000 tokens of
+    K = 8, or 20 000 of K = 16, the kernel for any K): `down` holds 2.29
+    billion bf16 values (4.6 GB), and the restore order is a random
     permutation, so sampled tokens gather rows on both sides of element 2^31."""
     moe = _moe()
-    T, K, H = 40000, 8, 7168
+    T, H = 320000 // K, 7168
     N = T * K
     assert N * H > TWO31
     gen = torch.Generator(device="cuda").manual_seed(20232)
