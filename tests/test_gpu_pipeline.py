@@ -136,3 +136,35 @@ def test_cuda_graph_replay(name, fused):
     d_d.view(torch.int16).copy_(torch.from_numpy(down2.view(np.int16)))
     graph.replay()
     check(ids2, w2, idx2, fin2)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["route_index", "separate"])
+def test_concurrent_pipelines_on_two_streams(fused):
+    """Two pipelines (their own buffers and workspaces) enqueued in alternation
+    on two streams, four batches each, so that their kernels can run at the
+    same time: the library keeps no shared device state on these paths, and
+    every batch matches the oracle chain."""
+    names = ("dsv3_decode", "skewed_ungrouped")
+    runs = []
+    for name in names:
+        cfg, scores, bias, *_ = workload(name)
+        down = workload_down(name)
+        runs.append(dict(
+            name=name, pipe=_pipe(cfg, fused), stream=torch.cuda.Stream(),
+            s=torch.from_numpy(scores).cuda(), b=torch.from_numpy(bias).cuda(),
+            d=torch.from_numpy(down.view(np.int16)).cuda().view(torch.bfloat16),
+            outs=[torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+                  for _ in range(4)]))
+    torch.cuda.synchronize()
+    for i in range(4):
+        for r in runs:
+            r["stream"].wait_stream(torch.cuda.current_stream())
+            r["pipe"].route_and_index(r["s"], r["b"], r["stream"])
+            r["pipe"].finalize(r["d"], r["stream"], output=r["outs"][i])
+    torch.cuda.synchronize()
+    for r in runs:
+        want = f32_to_bf16_bits(workload_finalize_ref(r["name"]))
+        for out in r["outs"]:
+            assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), want), \
+                r["name"]
+        assert r["pipe"].device_status() == 0
