@@ -8,10 +8,10 @@
 //
 // HBM-bound: per token it streams K rows of 2H bytes from scattered
 // positions of `down` and writes one 2H-byte row. Each thread owns 16-byte
-// column chunks (8 bf16) of the current token and issues all K row loads of a
-// chunk (two chunks per iteration) before the fp32 FMA chain, so every SM
-// keeps many independent 16-byte loads in flight. Loads bypass L1 (each byte
-// is used once), stores are streaming.
+// column chunks (8 bf16) of the current token and issues all K row loads of
+// several chunks (four per iteration in the 128-thread kernel) before the
+// fp32 FMA chain, so every SM keeps many independent 16-byte loads in flight.
+// Loads bypass L1 (each byte is used once), stores are streaming.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -20,7 +20,14 @@ namespace moe {
 namespace {
 
 constexpr int kFinThreads = 128;
-constexpr int kChunkUnroll = 2;
+// Chunks per thread and iteration: 4 in the 128-thread kernels (K = 2: 8
+// loads of 16 bytes in flight per thread; K = 8: 32 loads, 164 registers,
+// three CTAs per SM). Two chunks measured 7.5% slower with K = 2 (491 against
+// 454 us, 131 072 tokens, H = 4096) and 1% slower with K = 8 (298.1 against
+// 294.8 us, 16 384 tokens, H = 7168); six or eight were slower again. The
+// wider CTAs of small batches keep 2 (at 512 threads 4 would spill).
+constexpr int kChunkUnroll = 4;
+constexpr int kChunkUnrollWide = 2;
 
 struct FinArgs {
   void* out;           // [T, H] bf16 or fp32
@@ -85,10 +92,11 @@ __device__ __forceinline__ void store_chunk(void* out, int64_t t, int64_t H8, in
   }
 }
 
-// K known at compile time: all K row loads of kChunkUnroll chunks in flight.
+// K known at compile time: all K row loads of kUnroll chunks in flight.
 // kThreads per CTA (one CTA per token): kFinThreads, or more for small
 // batches so that a token's row takes fewer dependent rounds of loads.
-template <int K, typename WT, typename OT, int kThreads = kFinThreads>
+template <int K, typename WT, typename OT, int kThreads = kFinThreads,
+          int kUnroll = kChunkUnroll>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   wait_for_prior_grid();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
@@ -105,17 +113,17 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
       w[k] = load_weight<WT>(a.weight, t * K + k);
     }
     if (!all_ok && threadIdx.x == 0) report_bad_restore(a.status);
-    for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kThreads * kChunkUnroll) {
-      uint4 v[kChunkUnroll][K];
+    for (int64_t c0 = threadIdx.x; c0 < a.H8; c0 += (int64_t)kThreads * kUnroll) {
+      uint4 v[kUnroll][K];
 #pragma unroll
-      for (int u = 0; u < kChunkUnroll; ++u) {
+      for (int u = 0; u < kUnroll; ++u) {
         const int64_t c = c0 + (int64_t)u * kThreads;
 #pragma unroll
         for (int k = 0; k < K; ++k)
           v[u][k] = (c < a.H8 && ok[k]) ? load_stream(a.down + row[k] + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < kChunkUnroll; ++u) {
+      for (int u = 0; u < kUnroll; ++u) {
         const int64_t c = c0 + (int64_t)u * kThreads;
         if (c >= a.H8) break;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -183,21 +191,22 @@ moe_status_t launch_fin(Kernel k, const FinArgs& a, cudaStream_t stream,
   return launch(k, grid, threads, 0, stream, a);
 }
 
-// K fixed at compile time. When a row needs more than one round of loads at
-// kFinThreads threads, a batch with at most one token per SM takes up to 512
-// threads per token and one with at most two up to 256 (still one wave of
-// CTAs at the registers a thread holds): a decode token's row of H = 7168
-// then takes one round instead of four, and a decode step (route + index +
-// finalize, 128 tokens, replayed from a CUDA graph) measured 9.4 us against
-// 10.2 us. Short rows keep kFinThreads (more threads only idled there).
+// K fixed at compile time. When one round of loads at two chunks per thread
+// needs more than kFinThreads threads, a batch with at most one token per SM
+// takes up to 512 threads per token and one with at most two up to 256 (two
+// chunks per thread; still one wave of CTAs at the registers a thread
+// holds): a decode token's row of H = 7168 then takes one round, and a decode
+// step (route + index + finalize, 128 tokens, replayed from a CUDA graph)
+// measured 9.4 us against 10.2 us with 128 threads. Short rows and larger
+// batches take the 128-thread kernel.
 template <int K, typename WT, typename OT>
 moe_status_t launch_fin_k(const FinArgs& a, cudaStream_t stream) {
   const int64_t sms = device_info().sm_count;
-  const int64_t one_round = (a.H8 + kChunkUnroll - 1) / kChunkUnroll;  // threads
+  const int64_t one_round = (a.H8 + kChunkUnrollWide - 1) / kChunkUnrollWide;  // threads
   if (one_round > 256 && a.T <= sms)
-    return launch_fin(finalize_kernel<K, WT, OT, 512>, a, stream, 512);
+    return launch_fin(finalize_kernel<K, WT, OT, 512, kChunkUnrollWide>, a, stream, 512);
   if (one_round > kFinThreads && a.T <= 2 * sms)
-    return launch_fin(finalize_kernel<K, WT, OT, 256>, a, stream, 256);
+    return launch_fin(finalize_kernel<K, WT, OT, 256, kChunkUnrollWide>, a, stream, 256);
   return launch_fin(finalize_kernel<K, WT, OT>, a, stream);
 }
 
