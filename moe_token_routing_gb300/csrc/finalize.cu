@@ -135,7 +135,12 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   }
 }
 
-// Any K <= 32: one row load per step, chunks unrolled for some overlap.
+// Any K <= 32: the rows go in blocks of kKBlock, all row loads of a block
+// (kChunkUnroll chunks each) in flight before its FMAs, which keep k
+// ascending. One row at a time (four loads in flight per thread) measured
+// 393.4 us for K = 16 over 8192 tokens of H = 7168.
+constexpr int kKBlock = 4;
+
 template <typename WT, typename OT>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinArgs a) {
   wait_for_prior_grid();
@@ -146,22 +151,33 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel_any_k(const FinAr
       for (int u = 0; u < kChunkUnroll; ++u)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
-      for (int k = 0; k < a.K; ++k) {
-        const uint32_t r = __ldg(a.restore + t * a.K + k);
-        const float w = load_weight<WT>(a.weight, t * a.K + k);
-        if (r >= a.N) {
-          if (threadIdx.x == 0 && c0 == 0) report_bad_restore(a.status);
-          continue;
-        }
-        const uint4* src = a.down + (int64_t)r * a.H8;
-        uint4 v[kChunkUnroll];
+      for (int kb = 0; kb < a.K; kb += kKBlock) {
+        uint4 v[kKBlock][kChunkUnroll];
+        float w[kKBlock];
+        bool use[kKBlock];
 #pragma unroll
-        for (int u = 0; u < kChunkUnroll; ++u) {
-          const int64_t c = c0 + (int64_t)u * kFinThreads;
-          v[u] = c < a.H8 ? load_stream(src + c) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kKBlock; ++j) {
+          const int k = kb + j;
+          use[j] = k < a.K;
+          const uint32_t r = use[j] ? __ldg(a.restore + t * a.K + k) : 0u;
+          w[j] = use[j] ? load_weight<WT>(a.weight, t * a.K + k) : 0.0f;
+          if (use[j] && r >= a.N) {
+            if (threadIdx.x == 0 && c0 == 0) report_bad_restore(a.status);
+            use[j] = false;
+          }
+          const uint4* src = a.down + (int64_t)(use[j] ? r : 0u) * a.H8;
+#pragma unroll
+          for (int u = 0; u < kChunkUnroll; ++u) {
+            const int64_t c = c0 + (int64_t)u * kFinThreads;
+            v[j][u] = (use[j] && c < a.H8) ? load_stream(src + c) : make_uint4(0, 0, 0, 0);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < kChunkUnroll; ++u) fma_bf16x8(acc[u], w, v[u]);
+        for (int j = 0; j < kKBlock; ++j) {
+          if (!use[j]) continue;
+#pragma unroll
+          for (int u = 0; u < kChunkUnroll; ++u) fma_bf16x8(acc[u], w[j], v[j][u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kChunkUnroll; ++u) {
