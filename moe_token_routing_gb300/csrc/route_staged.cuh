@@ -159,12 +159,20 @@ __device__ __forceinline__ uint32_t staged_key_nonneg(float b, uint32_t key_low,
   return (__float_as_uint(b) & ~key_low) ^ tag;
 }
 
+// Index bits of the selection keys for E experts (the host's rule: the
+// smallest b >= 1 with 2^b >= E), fixed at compile time in the staged
+// kernels, where E = 32 * G.
+__host__ __device__ constexpr int staged_key_bits(int E) {
+  int b = 1;
+  while ((1 << b) < E) ++b;
+  return b;
+}
+
 // The descending top-8 selection keys of kept group `grp` of the token whose
 // staged row is `row` (32 experts, read at the rotated columns of this lane).
-template <bool kNonneg>
-__device__ __forceinline__ void staged_group_top8(const RouteArgs& a, const float* row,
-                                                  const float* s_bias, int grp, int rot,
-                                                  uint32_t (&top)[8]) {
+template <bool kNonneg, uint32_t kKeyLow>
+__device__ __forceinline__ void staged_group_top8(const float* row, const float* s_bias, int grp,
+                                                  int rot, uint32_t (&top)[8]) {
   uint32_t key[4][8];
   const float* rg = row + grp * 32;
   const float* bg = s_bias + grp * 32;
@@ -178,16 +186,16 @@ __device__ __forceinline__ void staged_group_top8(const RouteArgs& a, const floa
     const float b2 = __fadd_rn(v.z, bb.z), b3 = __fadd_rn(v.w, bb.w);
     uint32_t* k = &key[c >> 1][(c & 1) * 4];
     if constexpr (kNonneg) {
-      const uint32_t tag = 0x80000000u | (a.key_low - (uint32_t)e);
-      k[0] = staged_key_nonneg(b0, a.key_low, tag);
-      k[1] = staged_key_nonneg(b1, a.key_low, tag - 1u);
-      k[2] = staged_key_nonneg(b2, a.key_low, tag - 2u);
-      k[3] = staged_key_nonneg(b3, a.key_low, tag - 3u);
+      const uint32_t tag = 0x80000000u | (kKeyLow - (uint32_t)e);
+      k[0] = staged_key_nonneg(b0, kKeyLow, tag);
+      k[1] = staged_key_nonneg(b1, kKeyLow, tag - 1u);
+      k[2] = staged_key_nonneg(b2, kKeyLow, tag - 2u);
+      k[3] = staged_key_nonneg(b3, kKeyLow, tag - 3u);
     } else {
-      k[0] = staged_key(b0, a.key_low, e + 0);
-      k[1] = staged_key(b1, a.key_low, e + 1);
-      k[2] = staged_key(b2, a.key_low, e + 2);
-      k[3] = staged_key(b3, a.key_low, e + 3);
+      k[0] = staged_key(b0, kKeyLow, e + 0);
+      k[1] = staged_key(b1, kKeyLow, e + 1);
+      k[2] = staged_key(b2, kKeyLow, e + 2);
+      k[3] = staged_key(b3, kKeyLow, e + 3);
     }
   }
 #pragma unroll
@@ -200,13 +208,13 @@ __device__ __forceinline__ void staged_group_top8(const RouteArgs& a, const floa
 }
 
 // Best key below `last` in kept group `grp` (0 if none).
-__device__ __forceinline__ uint32_t staged_group_best_below(const RouteArgs& a, const float* row,
-                                                            const float* s_bias, int grp,
-                                                            uint32_t last) {
+template <uint32_t kKeyLow>
+__device__ __forceinline__ uint32_t staged_group_best_below(const float* row, const float* s_bias,
+                                                            int grp, uint32_t last) {
   uint32_t best = 0u;
   for (int i = 0; i < 32; ++i) {
     const int e = grp * 32 + i;
-    const uint32_t k = staged_key(__fadd_rn(row[e], s_bias[e]), a.key_low, e);
+    const uint32_t k = staged_key(__fadd_rn(row[e], s_bias[e]), kKeyLow, e);
     best = k < last ? max(best, k) : best;
   }
   return best;
@@ -246,6 +254,8 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
   constexpr int kTok = 32 / R;           // tokens per chunk
   constexpr int kOut = kSegTop / R;      // list entries (picks) per thread
   constexpr int kRow = kTok * E;         // floats per chunk buffer
+  constexpr int kKeyBits = staged_key_bits(E);  // equal to a.key_bits (same rule)
+  constexpr uint32_t kKeyLow = (1u << kKeyBits) - 1u;
   const int W = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -504,9 +514,9 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
         my_grp[r] = use ? grp : -1;
         uint32_t lst[8];
         if (nonneg)
-          staged_group_top8<true>(a, row, s_bias, grp, rot, lst);
+          staged_group_top8<true, kKeyLow>(row, s_bias, grp, rot, lst);
         else
-          staged_group_top8<false>(a, row, s_bias, grp, rot, lst);
+          staged_group_top8<false, kKeyLow>(row, s_bias, grp, rot, lst);
 #pragma unroll
         for (int i = 0; i < 8; ++i) lst[i] = use ? lst[i] : 0u;
         if (r == 0) {
@@ -544,7 +554,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
 #pragma unroll
         for (int r = 0; r < P; ++r)
           if (my_grp[r] >= 0)
-            next = max(next, staged_group_best_below(a, row, s_bias, my_grp[r], last));
+            next = max(next, staged_group_best_below<kKeyLow>(row, s_bias, my_grp[r], last));
       }
 #pragma unroll
       for (int off = 1; off < R; off <<= 1)
@@ -558,7 +568,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     for (int r = 0; r < kSegTop; ++r) {
       if (r < K) {
         const uint32_t nx = r + 1 < K ? top[r + 1 < 8 ? r + 1 : 7] : next;
-        redo = redo || ((top[r] ^ nx) >> a.key_bits) == 0u;
+        redo = redo || ((top[r] ^ nx) >> kKeyBits) == 0u;
       }
     }
 
@@ -566,16 +576,16 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
     int id[kOut];
 #pragma unroll
     for (int o = 0; o < kOut; ++o)
-      id[o] = (int)(a.key_low - (pick_for_thread<R, kOut>(top, h, o) & a.key_low));
+      id[o] = (int)(kKeyLow - (pick_for_thread<R, kOut>(top, h, o) & kKeyLow));
 
     // ---- ties: rank the candidates by their exact keys (see the segment layout) ----
     bool exact_path = redo && last == 0u;
     if (__any_sync(kFullMask, redo && !exact_path)) {
-      const bool boundary = ((last ^ next) >> a.key_bits) == 0u;
-      const uint32_t hk = (boundary ? next : last) >> a.key_bits;
+      const bool boundary = ((last ^ next) >> kKeyBits) == 0u;
+      const uint32_t hk = (boundary ? next : last) >> kKeyBits;
       int c = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c += mine[i] != 0u && (mine[i] >> a.key_bits) >= hk;
+      for (int i = 0; i < 8; ++i) c += mine[i] != 0u && (mine[i] >> kKeyBits) >= hk;
       const bool over = boundary && c == 8;
       if (!redo || exact_path) c = 0;
       int incl = c;  // this thread's end offset in the token's candidate list
@@ -591,11 +601,11 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (i < c) {
-          const int e = (int)(a.key_low - (mine[i] & a.key_low));
+          const int e = (int)(kKeyLow - (mine[i] & kKeyLow));
           const float b = __fadd_rn(row[e], s_bias[e]);
           const uint32_t u = __float_as_uint(b);
           const uint32_t tk = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-          tok_cand[incl - c + i] = ((uint64_t)tk << 32) | (a.key_low - (uint32_t)e);
+          tok_cand[incl - c + i] = ((uint64_t)tk << 32) | (kKeyLow - (uint32_t)e);
         }
       }
       __syncwarp();
@@ -605,7 +615,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
           const uint64_t x = tok_cand[incl - c + i];
           int r = 0;
           for (int m = 0; m < n; ++m) r += tok_cand[m] > x;  // keys are distinct
-          if (r < K) tok_slot[r] = (int)(a.key_low - (uint32_t)(x & 0xffffffffull));
+          if (r < K) tok_slot[r] = (int)(kKeyLow - (uint32_t)(x & 0xffffffffull));
         }
       }
       __syncwarp();
