@@ -442,10 +442,20 @@ __device__ __forceinline__ uint32_t pick8(const uint32_t (&x)[8], int i) {
 // Selection key of a biased score b that is not -0 (the staged bias holds no
 // -0, and x + y is -0 only when both are -0), so the order key needs no
 // zero fold.
-__device__ __forceinline__ uint32_t selection_key(const RouteArgs& a, float b, uint32_t tag) {
+template <uint32_t kKeyLow>
+__device__ __forceinline__ uint32_t selection_key(float b, uint32_t tag) {
   const uint32_t u = __float_as_uint(b);
   const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-  return (k & ~a.key_low) | tag;
+  return (k & ~kKeyLow) | tag;
+}
+
+// Index bits of the selection keys for E experts: the smallest b >= 1 with
+// 2^b >= E. plan_route sets RouteArgs::key_bits with it, and the layouts that
+// know E at compile time (segment, staged) use it as a constant.
+__host__ __device__ constexpr int key_bits_for(int E) {
+  int b = 1;
+  while ((1 << b) < E) ++b;
+  return b;
 }
 
 // The routing score of one expert from its loaded value x: the score
@@ -555,7 +565,9 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
   const int e0 = kSegKeys * j;
   uint64_t* seg_cand = cand + (lane / L) * kSegCand;
   int* seg_slot = slot + (lane / L) * kSegTop;
-  const uint32_t tag0 = a.key_low - (uint32_t)e0;
+  constexpr int kKeyBits = key_bits_for(kSegKeys * L);  // E = 32 * L here
+  constexpr uint32_t kKeyLow = (1u << kKeyBits) - 1u;
+  const uint32_t tag0 = kKeyLow - (uint32_t)e0;
   const int gl = kGroups ? L / a.G : L;  // lanes per group
   const int grp = j / gl;
   const float* bias_j = s_bias + kSegBiasStride * j;
@@ -598,7 +610,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
       add_seg_bias(bias_j, b);
 #pragma unroll
       for (int i = 0; i < kSegKeys; ++i) {
-        key[i / 8][i % 8] = selection_key(a, b[i], tag0 - (uint32_t)i);
+        key[i / 8][i % 8] = selection_key<kKeyLow>(b[i], tag0 - (uint32_t)i);
         if constexpr (kGroups) top2_push(t1, t2, b[i]);
       }
     }
@@ -662,7 +674,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
         add_seg_bias(bias_j, b);
 #pragma unroll
         for (int i = 0; i < kSegKeys; ++i) {
-          const uint32_t k = selection_key(a, b[i], tag0 - (uint32_t)i);
+          const uint32_t k = selection_key<kKeyLow>(b[i], tag0 - (uint32_t)i);
           next = k < last ? max(next, k) : next;
         }
       }
@@ -677,14 +689,14 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
     for (int r = 0; r < kSegTop; ++r) {
       if (r < a.K) {
         const uint32_t nx = r + 1 < a.K ? top[r + 1 < 8 ? r + 1 : 7] : next;
-        redo = redo || ((top[r] ^ nx) >> a.key_bits) == 0u;
+        redo = redo || ((top[r] ^ nx) >> kKeyBits) == 0u;
       }
     }
 
     // ---- ids (list entries j, j + L, ...) ----
     int id[kOut];
 #pragma unroll
-    for (int o = 0; o < kOut; ++o) id[o] = (int)(a.key_low - (pick8(top, j + L * o) & a.key_low));
+    for (int o = 0; o < kOut; ++o) id[o] = (int)(kKeyLow - (pick8(top, j + L * o) & kKeyLow));
 
     // ---- ties: rank the candidates by their exact keys ----
     // Let h be the high part of the (K+1)-th key, or of the K-th when the
@@ -695,11 +707,11 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
     // (order key, then expert) give each one's rank, hence its position.
     bool exact_path = redo && last == 0u;  // fewer than K candidates: the warp path decides
     if (__any_sync(kFullMask, redo && !exact_path)) {
-      const bool boundary = ((last ^ next) >> a.key_bits) == 0u;
-      const uint32_t h = (boundary ? next : last) >> a.key_bits;
+      const bool boundary = ((last ^ next) >> kKeyBits) == 0u;
+      const uint32_t h = (boundary ? next : last) >> kKeyBits;
       int c = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c += mine[i] != 0u && (mine[i] >> a.key_bits) >= h;
+      for (int i = 0; i < 8; ++i) c += mine[i] != 0u && (mine[i] >> kKeyBits) >= h;
       const bool over = boundary && c == 8;
       if (!redo || exact_path) c = 0;
       int incl = c;  // this lane's end offset in the segment's candidate list
@@ -716,11 +728,11 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (i < c) {
-          const int e = (int)(a.key_low - (mine[i] & a.key_low));
+          const int e = (int)(kKeyLow - (mine[i] & kKeyLow));
           const float b = __fadd_rn(seg_score<kSoftmax>(a, __ldg(row + e), smax, ssum), bias_j[e - e0]);
           const uint32_t u = __float_as_uint(b);
           const uint32_t tk = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-          seg_cand[incl - c + i] = ((uint64_t)tk << 32) | (a.key_low - (uint32_t)e);
+          seg_cand[incl - c + i] = ((uint64_t)tk << 32) | (kKeyLow - (uint32_t)e);
         }
       }
       __syncwarp();
@@ -730,7 +742,7 @@ __device__ __forceinline__ void route_tokens_seg(const RouteArgs& a, const float
           const uint64_t x = seg_cand[incl - c + i];
           int r = 0;
           for (int m = 0; m < n; ++m) r += seg_cand[m] > x;  // keys are distinct
-          if (r < a.K) seg_slot[r] = (int)(a.key_low - (uint32_t)(x & 0xffffffffull));
+          if (r < a.K) seg_slot[r] = (int)(kKeyLow - (uint32_t)(x & 0xffffffffull));
         }
       }
       __syncwarp();
@@ -953,8 +965,7 @@ inline moe_status_t plan_route(int32_t* expert_indices, float* expert_weights,
   a.score_fn = score_fn;
   a.warp_smem_words = 0;
   a.softmax_off = 0;
-  a.key_bits = 1;
-  while ((1 << a.key_bits) < E) ++a.key_bits;
+  a.key_bits = key_bits_for(E);
   a.key_low = (1u << a.key_bits) - 1u;
   p->seg = 0;
   p->staged = 0;

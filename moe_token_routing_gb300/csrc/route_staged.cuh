@@ -159,15 +159,6 @@ __device__ __forceinline__ uint32_t staged_key_nonneg(float b, uint32_t key_low,
   return (__float_as_uint(b) & ~key_low) ^ tag;
 }
 
-// Index bits of the selection keys for E experts (the host's rule: the
-// smallest b >= 1 with 2^b >= E), fixed at compile time in the staged
-// kernels, where E = 32 * G.
-__host__ __device__ constexpr int staged_key_bits(int E) {
-  int b = 1;
-  while ((1 << b) < E) ++b;
-  return b;
-}
-
 // The descending top-8 selection keys of kept group `grp` of the token whose
 // staged row is `row` (32 experts, read at the rotated columns of this lane).
 template <bool kNonneg, uint32_t kKeyLow>
@@ -254,7 +245,7 @@ __device__ __forceinline__ void route_tokens_staged(const RouteArgs& a, char* sm
   constexpr int kTok = 32 / R;           // tokens per chunk
   constexpr int kOut = kSegTop / R;      // list entries (picks) per thread
   constexpr int kRow = kTok * E;         // floats per chunk buffer
-  constexpr int kKeyBits = staged_key_bits(E);  // equal to a.key_bits (same rule)
+  constexpr int kKeyBits = key_bits_for(E);  // equal to a.key_bits (the same function)
   constexpr uint32_t kKeyLow = (1u << kKeyBits) - 1u;
   const int W = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
