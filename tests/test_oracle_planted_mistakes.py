@@ -85,6 +85,28 @@ MUTANTS = {
         "for (int32_t k = 1; k < K; ++k) sum = sum + w[k];"),
     "CSR starts one past": ("expert_start_indices[active] = offset;",
                             "expert_start_indices[active] = offset + 1;"),
+    "group limit ignored": (
+        "for (int32_t m = 0; m < topk_group; ++m) {", "for (int32_t m = 0; m < n_groups; ++m) {"),
+    "experts ranked by the unbiased score": (
+        "if (b[x] != b[y]) return b[x] > b[y];\n      return x < y;",
+        "if (s[x] != s[y]) return s[x] > s[y];\n      return x < y;"),
+    "scaling before the normalisation": (
+        "    if (norm_weights) {\n      float sum = 0.0f;\n"
+        "      for (int32_t k = 0; k < K; ++k) sum = sum + w[k];\n"
+        "      for (int32_t k = 0; k < K; ++k) w[k] = w[k] / sum;\n    }\n"
+        "    for (int32_t k = 0; k < K; ++k) w[k] = w[k] * scale;",
+        "    for (int32_t k = 0; k < K; ++k) w[k] = w[k] * scale;\n"
+        "    if (norm_weights) {\n      float sum = 0.0f;\n"
+        "      for (int32_t k = 0; k < K; ++k) sum = sum + w[k];\n"
+        "      for (int32_t k = 0; k < K; ++k) w[k] = w[k] / sum;\n    }"),
+    "sigmoid of the negated logit": ("out[i] = 1.0f / (1.0f + exp_cody_waite(-x[i]));",
+                                     "out[i] = 1.0f / (1.0f + exp_cody_waite(x[i]));"),
+    "scale offsets for idle experts too": (
+        "    if (count[e] == 0) continue;\n    out[j++] = static_cast<uint32_t>(offset);",
+        "    out[j++] = static_cast<uint32_t>(offset);"),
+    "scale offsets tail left at zero": (
+        "for (; j <= E; ++j) out[j] = static_cast<uint32_t>(offset);",
+        "for (; j <= E; ++j) out[j] = 0u;"),
     "expert_ids tail padded with 0": ("for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
                                       "expert_ids[j] = -1;",
                                       "for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
