@@ -107,6 +107,18 @@ MUTANTS = {
     "scale offsets tail left at zero": (
         "for (; j <= E; ++j) out[j] = static_cast<uint32_t>(offset);",
         "for (; j <= E; ++j) out[j] = 0u;"),
+    "stats max taken from the last expert": ("max_count = std::max(max_count, count[e]);",
+                                             "max_count = count[e];"),
+    "active experts walked in descending id": (
+        "for (int32_t e = 0; e < E; ++e) {\n    max_count",
+        "for (int32_t e = E - 1; e >= 0; --e) {\n    max_count"),
+    "permute ignores token_expert_order": ("const int64_t slot = token_expert_order[p];",
+                                           "const int64_t slot = p;"),
+    "fp64 finalize drops the weights": ("acc += static_cast<double>(w[t * K + k]) *",
+                                        "acc += 1.0 *"),
+    "selected-token finalize ignores the selection": (
+        "int rc = finalize_one_token(down, restore, w, T, K, H, tokens[j], out + j * H);",
+        "int rc = finalize_one_token(down, restore, w, T, K, H, j, out + j * H);"),
     "expert_ids tail padded with 0": ("for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
                                       "expert_ids[j] = -1;",
                                       "for (uint32_t j = active; j < static_cast<uint32_t>(E); ++j) "
@@ -133,6 +145,8 @@ def _pins():
         lambda: tf.test_library_gather_weighted_sum(33, 8, 256),
         lambda: tf.test_library_gather_weighted_sum(17, 3, 72),
         tf.test_tiny_workload_chain,
+        tf.test_fp64_variant_bounds_fp32,
+        tf.test_selected_tokens_match_full,
         tp.test_golden_fixture,
         lambda: tp.test_library_gather(64, 4, 24),
         lambda: tp.test_round_trip_through_finalize(2),
