@@ -10,7 +10,8 @@ from .binding import (DEVICE_STATUS_BAD_EXPERT_ID, DEVICE_STATUS_BAD_RESTORE_ORD
                       DEVICE_STATUS_SYNC_TIMEOUT, EXPORTED_SYMBOLS, SCORES_AS_GIVEN,
                       SCORES_SIGMOID, SCORES_SOFTMAX, IndexBuffers, MoeError, MoeLibraryMissing,
                       RouteIndexBuffers, create_indices, finalize, load_library,
-                      moe_create_indices, moe_create_indices_workspace_size, moe_finalize,
+                      moe_create_indices, moe_create_indices_no_alloc,
+                      moe_create_indices_workspace_size, moe_finalize,
                       moe_finalize_ex, moe_permute, moe_read_device_status, moe_route,
                       moe_route_ex, moe_route_index, moe_route_index_single_launch_workspace_size,
                       moe_route_index_workspace_size, permute,
@@ -23,7 +24,8 @@ __all__ = [
     "EXPORTED_SYMBOLS", "RouteIndexBuffers", "moe_route_index", "moe_route_index_workspace_size",
     "moe_route_index_single_launch_workspace_size", "route_index", "HostStreamer", "IndexBuffers", "MoeError",
     "MoeLibraryMissing", "RoutingPipeline", "create_indices", "finalize", "load_library",
-    "moe_create_indices", "moe_create_indices_workspace_size", "moe_finalize",
+    "moe_create_indices", "moe_create_indices_no_alloc", "moe_create_indices_workspace_size",
+    "moe_finalize",
     "moe_finalize_ex", "moe_permute", "moe_read_device_status", "moe_route", "moe_route_ex",
     "permute", "route", "SCORES_AS_GIVEN", "SCORES_SIGMOID", "SCORES_SOFTMAX",
 ]
